@@ -1,0 +1,407 @@
+"""Benchmark of the vocab-wide sampling pass (libdsample) -- prints ONE JSON line on rank 0.
+
+Default workload: the throughput configuration -- 64 requests, C = 8 rows, ragged
+T ~ U{100..400} positions (P = 15510, 124080 cells), V = 1025, bf16 c and u,
+guidance 2, temperature 0.9, top ratio 0.1, seed 2. One step = one ds_sample call
+over the whole batch (iteration counter = step index mod 32). Inputs are 510 MB,
+far above the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload cfg3|cfg5|cfg4|cfg1|cfg2] [--no-extra]
+
+Under torchrun (N > 1) every rank runs its own full batch (weak scaling: cells are
+independent, no collective on the data path); the timed region is bracketed by
+barriers and the max over ranks is reported.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["ds_device.cuh", "ds_sample_common.cuh", "k_sample_warp.cu", "k_sample_cluster.cu",
+                  "k_greedy.cu", "ds_api.cu"]
+
+
+# ------------------------------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+            if key in d and d[key]:
+                return float(d[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "vocab_wide_logit_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_workload(name):
+    from vocab_wide_logit_gb300 import workloads as wl
+    if name == "cfg4":
+        return wl.config4()
+    return wl.SAMPLE_CONFIGS[name]()
+
+
+class SampleRunner:
+    def __init__(self, inp, dev):
+        import vocab_wide_logit_gb300 as pkg
+        self.pkg = pkg
+        self.inp = inp
+        self.rid = torch.from_numpy(inp.request_ids).to(dev)
+        self.sl = torch.from_numpy(inp.seq_lens.astype(np.int32)).to(dev)
+        self.g = torch.from_numpy(inp.guidance).to(dev)
+        self.tau = torch.from_numpy(inp.temperature).to(dev)
+        self.c = inp.c_logits.to(dev)
+        self.u = inp.u_logits.to(dev) if inp.u_logits is not None else None
+        self.tok = torch.empty((inp.C, inp.P), dtype=torch.int32, device=dev)
+        self.lp = torch.empty((inp.C, inp.P), dtype=torch.float32, device=dev)
+
+    def step(self, i):
+        self.pkg.ds_sample(self.rid, self.c, self.u, self.sl, self.g, self.tau, self.inp.top_ratio,
+                           self.inp.seed, i % 32, self.tok, self.lp)
+
+    units = property(lambda self: self.inp.cells)
+    bytes_per_step = property(lambda self: self.inp.algorithmic_bytes())
+
+
+class GreedyRunner:
+    """Rotates 4 input buffers (4 x 127 MB > L2) so that no call is served from L2."""
+
+    def __init__(self, g, dev, n_buf=4):
+        import vocab_wide_logit_gb300 as pkg
+        self.pkg = pkg
+        self.g = g
+        base = g.logits.to(dev)
+        self.bufs = [base] + [base.roll(j + 1, dims=0).contiguous() for j in range(n_buf - 1)]
+        self.mx = torch.empty(g.n, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(g.n, dtype=torch.float32, device=dev)
+        self.am = torch.empty(g.n, dtype=torch.int32, device=dev)
+
+    def step(self, i):
+        self.pkg.ds_greedy_lse(self.bufs[i % len(self.bufs)], self.mx, self.lse, self.am)
+
+    units = property(lambda self: self.g.n)
+    bytes_per_step = property(lambda self: self.g.algorithmic_bytes())
+
+
+def time_steps(runner, steps, warmup, world):
+    for i in range(warmup):
+        runner.step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(steps):
+        runner.step(warmup + i)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    return ms / steps
+
+
+def oracle_cpu_rate(inp, max_seconds=10.0, iteration=0):
+    """Run the CPU oracle (single thread) on a bounded sample of the workload's cells.
+    Returns (cells per second, sample description, cells)."""
+    import oracle
+    from vocab_wide_logit_gb300 import workloads as wl
+    cb = wl.bf16_bits(inp.c_logits)
+    ub = wl.bf16_bits(inp.u_logits) if inp.u_logits is not None else None
+    n = inp.cells
+    # calibrate on a small strided sample, then size the timed sample to about max_seconds
+    cal = np.arange(0, n, max(1, n // 200), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.sample_cells(inp.request_ids, cb, ub, inp.seq_lens, inp.C, inp.P, inp.V, inp.guidance,
+                        inp.temperature, inp.top_ratio, inp.seed, iteration, cal)
+    per = (time.perf_counter() - t0) / len(cal)
+    want = int(min(n, max(len(cal), max_seconds / max(per, 1e-9))))
+    cells = np.linspace(0, n - 1, want).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.sample_cells(inp.request_ids, cb, ub, inp.seq_lens, inp.C, inp.P, inp.V, inp.guidance,
+                        inp.temperature, inp.top_ratio, inp.seed, iteration, cells)
+    dt = time.perf_counter() - t0
+    return want / dt, "%d of %d cells (evenly spaced), iteration %d" % (want, n, iteration), want
+
+
+def oracle_cpu_rate_greedy(g, max_seconds=10.0):
+    import oracle
+    from vocab_wide_logit_gb300 import workloads as wl
+    bits = wl.bf16_bits(g.logits)
+    t0 = time.perf_counter()
+    oracle.greedy_rows(bits, g.n, g.V, np.arange(min(4, g.n), dtype=np.int64))
+    per = (time.perf_counter() - t0) / min(4, g.n)
+    want = int(min(g.n, max(1, max_seconds / max(per, 1e-9))))
+    rows = np.arange(want, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.greedy_rows(bits, g.n, g.V, rows)
+    dt = time.perf_counter() - t0
+    return want / dt, "%d of %d rows" % (want, g.n), want
+
+
+def e2e_rate(inp, dev, steps):
+    """Through the public API from pinned host memory: every step copies c (and u) host->device,
+    samples, and copies (tokens, logprobs) back."""
+    from vocab_wide_logit_gb300.api import HostSampler
+    hs = HostSampler(torch.from_numpy(inp.request_ids), torch.from_numpy(inp.seq_lens.astype(np.int32)),
+                     torch.from_numpy(inp.guidance), torch.from_numpy(inp.temperature), inp.C, inp.P, inp.P_u,
+                     inp.V, device=dev)
+    c_h = inp.c_logits.pin_memory()
+    u_h = inp.u_logits.pin_memory() if inp.u_logits is not None else None
+    for i in range(2):
+        hs(c_h, u_h, inp.top_ratio, inp.seed, i)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(steps):
+        hs(c_h, u_h, inp.top_ratio, inp.seed, i % 32)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return inp.cells / (ms / 1e3), hs.h2d_bytes(), hs.d2h_bytes()
+
+
+def roofline(bytes_per_step, ms, workload):
+    peak, src = hbm_peak()
+    ach = bytes_per_step / (ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "peak_source": src, "unit": "GB/s",
+            "frac": round(ach / peak, 4), "frac_of_8000": round(ach / 8000.0, 4),
+            "traffic": committed_traffic(workload), "algorithmic_bytes_per_launch": bytes_per_step}
+
+
+# ------------------------------------------------------------------------------------- arms
+def run_ours(args):
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import vocab_wide_logit_gb300 as pkg
+    pkg.load()
+    wname = args.workload
+    w = make_workload(wname)
+    is_greedy = wname == "cfg4"
+    runner = GreedyRunner(w, dev) if is_greedy else SampleRunner(w, dev)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[dev.index]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else dev.index
+    with ClockSampler(gpu_index) as clk:
+        ms = time_steps(runner, args.steps, args.warmup, world)
+    clocks = clk.summary()
+    units = runner.units * world
+    value = units / (ms / 1e3)
+    unit = "rows/s" if is_greedy else "sampled positions/s"
+    line = {
+        "metric": "greedy rows/s (max/LSE/argmax, V=248320)" if is_greedy else
+        "sampled positions/s (fused CFG + top-ratio + Gumbel, HBM roofline fraction alongside)",
+        "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded, bf16 inputs)",
+        "config": {"workload": w.name, "units_per_gpu_step": runner.units,
+                   "bytes_per_gpu_step": runner.bytes_per_step,
+                   "l2": "inputs larger than L2 (no flush)" if not is_greedy else
+                   "4 rotating input buffers, 508 MB total > L2",
+                   "parallelism": "dp%d (independent cells per rank)" % world},
+        "roofline": roofline(runner.bytes_per_step, ms, wname),
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not is_greedy:
+        line["logit_elements_per_s"] = round(value * w.V, 1)
+    if rank == 0:
+        # end to end through the public API, from pinned host memory
+        if not is_greedy:
+            ev, hb, db = e2e_rate(w, dev, max(3, min(args.steps, 10)))
+            line["e2e"] = {"value": round(ev * world, 1), "unit": unit, "h2d_bytes_per_step": hb,
+                           "d2h_bytes_per_step": db}
+        # the oracle on this host, bounded sample (N = 1 only)
+        if world > 1:
+            pass
+        elif is_greedy:
+            cv, sample, _ = oracle_cpu_rate_greedy(w, args.cpu_seconds)
+        else:
+            cv, sample, _ = oracle_cpu_rate(w, args.cpu_seconds)
+        if world == 1:
+            line["cpu_baseline"] = {"value": round(cv, 2), "unit": unit, "cores": 1, "kind": "oracle",
+                                    "sample": sample, "host_cpus": os.cpu_count()}
+        if not args.no_extra and wname == "cfg3" and world == 1:
+            extra = {}
+            for other in ("cfg5", "cfg4"):
+                del runner
+                torch.cuda.empty_cache()
+                ow = make_workload(other)
+                runner = GreedyRunner(ow, dev) if other == "cfg4" else SampleRunner(ow, dev)
+                oms = time_steps(runner, max(10, args.steps), args.warmup, 1)
+                extra[other] = {"workload": ow.name, "ms_per_step": round(oms, 5),
+                                "units_per_s": round(runner.units / (oms / 1e3), 1),
+                                "roofline": roofline(runner.bytes_per_step, oms, other)}
+                del ow
+            line["also"] = extra
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on this host's cores: each step samples a bounded slice of
+    the same workload; rank 0 alone under torchrun."""
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    wname = args.workload
+    w = make_workload(wname)
+    is_greedy = wname == "cfg4"
+    unit = "rows/s" if is_greedy else "sampled positions/s"
+    budget = max(1.0, args.ref_seconds_per_step)
+    rates = []
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        if is_greedy:
+            r, sample, _ = oracle_cpu_rate_greedy(w, budget)
+        else:
+            r, sample, _ = oracle_cpu_rate(w, budget, iteration=i % 32)
+        if i >= args.warmup:
+            rates.append(r)
+    value = statistics.median(rates)
+    line = {"impl": "reference", "metric": "sampled positions/s (fused CFG + top-ratio + Gumbel)"
+            if not is_greedy else "greedy rows/s (max/LSE/argmax, V=248320)",
+            "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded, bf16 inputs)",
+            "config": {"workload": w.name, "parallelism": "single host thread"},
+            "cpu_baseline": {"value": round(value, 2), "unit": unit, "cores": 1, "kind": "oracle",
+                             "sample": sample + " per step", "host_cpus": os.cpu_count()},
+            "e2e": {"value": round(value, 2), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["cfg3", "cfg5", "cfg4", "cfg1", "cfg2"], default="cfg3")
+    ap.add_argument("--no-extra", action="store_true", help="skip the large-vocab lines under 'also'")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds-per-step", type=float, default=3.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,134 @@
+/*
+ * dsample.h -- C ABI of libdsample, the GB300 (sm_103a) vocab-wide sampling pass.
+ *
+ * Two calls, both asynchronous on the caller's CUDA stream, both allocating
+ * nothing and keeping no state between calls:
+ *
+ *   ds_sample      classifier-free-guidance combine, full-vocab max / logsumexp,
+ *                  exact top-ratio filter and Gumbel-max sampling at per-request
+ *                  temperature; one (token, logprob) per (row, position) cell.
+ *   ds_greedy_lse  per-row max, logsumexp and argmax over a large vocabulary.
+ *
+ * All pointers named "device" must be CUDA device (or managed) memory of the
+ * current device; the library never frees or retains them. Inputs are never
+ * written. The stream argument is a cudaStream_t (NULL = legacy default
+ * stream). A host-side error is returned synchronously and nothing is
+ * launched; errors that only the GPU can see are reported through the
+ * optional device status word (see ds_sample).
+ */
+#ifndef DSAMPLE_H
+#define DSAMPLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DS_OK = 0,
+  DS_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad scalar */
+  DS_ERR_UNSUPPORTED = 2, /* valid but outside what this build supports (see limits) */
+  DS_ERR_CUDA = 3         /* a CUDA runtime call or the kernel launch failed */
+} ds_status;
+
+/* Bits OR-ed into *d_status by the kernels (device-detected input errors). */
+#define DS_DEV_ERR_LAYOUT 1u   /* sum(seq_lens) != P, or a negative seq_len */
+#define DS_DEV_ERR_NO_UNCOND 2u /* guidance != 0 for a request but u_logits == NULL */
+#define DS_DEV_ERR_PARAM 4u    /* temperature < 0 or NaN, or guidance NaN */
+
+/* Limits of this build. */
+#define DS_MAX_ROWS 256          /* C: rows (codebooks) per call; the row index keys the noise */
+#define DS_MAX_ITERATION 16777215u /* iteration < 2^24; it keys the noise next to the row */
+#define DS_MAX_VOCAB 262137      /* largest V of ds_sample (16-CTA cluster, 16K elements per CTA) */
+
+/*
+ * ds_sample -- sample every cell of a packed batch of guided logits.
+ *
+ * Defined by: "Sampler support for discrete diffusion" (mstar issue #267),
+ * Hert4's first comment (log-softmax, argmax and confidence per cell; logits
+ * [C, T, V] with T ragged across requests; CFG combine of two logit tensors;
+ * top-ratio filter keeping ceil(0.1 * V); Gumbel sampling; "sample every
+ * position handed in, return (tokens, logprobs)"), and "Add a sampler resource
+ * for discrete diffusion" (mstar PR #290), Contract (sample(request_ids,
+ * c_logits, u_logits, seq_lens, iterations) over [rows, positions, vocab]
+ * packed across requests; per-request guidance and temperature; no
+ * unconditional document at guidance 0).
+ *
+ * Arguments (B requests, C rows, P = sum of seq_lens positions, V vocabulary):
+ *   request_ids  device int32 [B]; any values; they key the noise of a request.
+ *   c_logits     device bf16 [C][P][V], V contiguous; request r owns positions
+ *                [off_r, off_r + seq_lens[r]) with off_r = sum_{j<r} seq_lens[j].
+ *                Needs 2-byte alignment only; rows may start anywhere.
+ *   u_logits     device bf16 [C][P_u][V], the unconditional logits of the
+ *                requests with guidance != 0 only, packed in request order
+ *                (P_u = sum of their seq_lens). NULL when no request is guided.
+ *   seq_lens     device int32 [B], each >= 0, summing to P.
+ *   B, C, P, V   B >= 0, 0 <= C <= DS_MAX_ROWS, P >= 0, 1 <= V <= DS_MAX_VOCAB.
+ *                C == 0 or P == 0 is a valid empty call (nothing launched).
+ *   guidance     device float [B]; per-request guidance g; z = c + g (c - u) in
+ *                fp32 (difference rounded, then one fma); g == 0 reads no u.
+ *   temperature  device float [B]; tau >= 0; tau == 0 returns the argmax.
+ *   top_ratio    (0, 1]; the kept set is the k = ceilf(top_ratio * V) largest z
+ *                (product in fp32, k clamped to [1, V]), ties at the cut kept
+ *                by smallest id.
+ *   seed         Philox4x32-10 key (low word, high word).
+ *   iteration    < 2^24; the denoising step; it keys the noise.
+ *   out_tokens   device int32 [C][P]: sampled token, argmax when tau == 0;
+ *                ties between equal perturbed scores go to the smallest id.
+ *   out_logprobs device float [C][P]: z[token] - logsumexp(z) over the full,
+ *                unfiltered, untempered vocabulary.
+ *   d_status     device uint32 word or NULL. Kernels OR DS_DEV_ERR_* bits into
+ *                it on input errors they detect; the affected cells get token
+ *                -1 and logprob NaN. The caller clears it.
+ *   stream       cudaStream_t.
+ *
+ * Noise: Gumbel G = -log(-log U) with U = ((x >> 8) + 1/2) 2^-24 and x word
+ * (id & 3) of Philox4x32-10(counter = (id >> 2, t, request_id, iteration << 8
+ * | row), key = (seed low, seed high)), t the request-local position.
+ * The token maximises z[id] + tau * G[id] over the kept set.
+ * Logits must be finite or -inf (no NaN, no +inf).
+ *
+ * Returns DS_OK, DS_ERR_INVALID_ARG, DS_ERR_UNSUPPORTED (V > DS_MAX_VOCAB,
+ * B beyond int32 cell counts) or DS_ERR_CUDA (launch failure).
+ */
+ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void* u_logits,
+                    const int32_t* seq_lens, int32_t B, int32_t C, int32_t P, int32_t V,
+                    const float* guidance, const float* temperature, float top_ratio,
+                    uint64_t seed, uint32_t iteration, int32_t* out_tokens, float* out_logprobs,
+                    uint32_t* d_status, void* stream);
+
+/*
+ * ds_greedy_lse -- per-row max, logsumexp and argmax of bf16 logits [n][V].
+ *
+ * Defined by: "perf: avoid full-vocab all-gather for draft greedy sampling"
+ * (LightLLM PR #1517), Design and invariants: each vocabulary shard yields
+ * its local max, log-sum-exp and argmax; ties go to the smallest token ID;
+ * the selected token's exact probability is exp(selected_logit -
+ * full_vocab_logsumexp), i.e. exp(out_max - out_lse) here. Inputs are not
+ * rewritten: the id and the normaliser are returned beside the logits.
+ *
+ * Arguments:
+ *   logits      device bf16 [n][V], V contiguous, 2-byte alignment.
+ *   n, V        n >= 0 (0: nothing launched), V >= 1.
+ *   out_max     device float [n]: max logit (exact).
+ *   out_lse     device float [n]: logsumexp over the row (fp32 accumulation).
+ *   out_argmax  device int32 [n]: smallest id attaining the max.
+ *   stream      cudaStream_t.
+ * Returns DS_OK, DS_ERR_INVALID_ARG or DS_ERR_CUDA.
+ */
+ds_status ds_greedy_lse(const void* logits, int32_t n, int32_t V, float* out_max, float* out_lse,
+                        int32_t* out_argmax, void* stream);
+
+/* Static description of a status code. Never NULL. */
+const char* ds_status_string(ds_status s);
+
+/* Kept count used by ds_sample: ceilf(top_ratio * V) in fp32, clamped to [1, V];
+ * 0 when the arguments are invalid. Host-only, no CUDA call. */
+int32_t ds_top_k(float top_ratio, int32_t V);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSAMPLE_H */

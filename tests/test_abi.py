@@ -1,0 +1,88 @@
+"""CPU checks of the C ABI: the library loads without a GPU, exports every symbol the public
+header declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+import vocab_wide_logit_gb300 as pkg
+from vocab_wide_logit_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from vocab_wide_logit_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(ds_[a-z_0-9]+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"ds_sample", "ds_greedy_lse", "ds_status_string", "ds_top_k"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(_lib.EXPORTED) == names
+
+
+def test_status_strings(lib):
+    for code in range(4):
+        assert pkg.status_string(code)
+    assert pkg.status_string(99) == "unknown status"
+
+
+def test_top_k_matches_oracle_definition(lib):
+    for V in (1, 2, 7, 100, 1025, 4097, 248320, 262137):
+        for ratio in (1e-7, 0.001, 0.05, 0.1, 0.25, 1 / 3, 0.5, 0.9, 0.999, 1.0):
+            assert pkg.top_k(ratio, V) == oracle.top_k(ratio, V), (ratio, V)
+    assert pkg.top_k(0.0, 10) == 0 and pkg.top_k(1.5, 10) == 0 and pkg.top_k(0.5, 0) == 0
+
+
+FAKE = ctypes.c_void_p(0x100000)  # never dereferenced: every call below fails validation first
+
+
+def _sample(lib, B=1, C=1, P=1, V=8, ratio=0.1, it=0, ptr=FAKE, c=FAKE):
+    return lib.ds_sample(ptr, c, None, ptr, B, C, P, V, ptr, ptr, ratio, 0, it, ptr, ptr, None, None)
+
+
+def test_host_side_argument_errors(lib):
+    assert _sample(lib, V=0) == _lib.DS_ERR_INVALID_ARG
+    assert _sample(lib, ratio=0.0) == _lib.DS_ERR_INVALID_ARG
+    assert _sample(lib, ratio=1.01) == _lib.DS_ERR_INVALID_ARG
+    assert _sample(lib, ratio=float("nan")) == _lib.DS_ERR_INVALID_ARG
+    assert _sample(lib, C=257) == _lib.DS_ERR_INVALID_ARG
+    assert _sample(lib, B=-1) == _lib.DS_ERR_INVALID_ARG
+    assert _sample(lib, it=1 << 24) == _lib.DS_ERR_INVALID_ARG
+    assert _sample(lib, B=0, P=3) == _lib.DS_ERR_INVALID_ARG
+    assert _sample(lib, ptr=None) == _lib.DS_ERR_INVALID_ARG
+    assert _sample(lib, c=ctypes.c_void_p(0x100001)) == _lib.DS_ERR_INVALID_ARG  # bf16 needs 2-byte alignment
+    assert _sample(lib, V=_lib.DS_MAX_VOCAB + 1) == _lib.DS_ERR_UNSUPPORTED
+    # empty calls are valid no-ops
+    assert _sample(lib, C=0) == _lib.DS_OK
+    assert _sample(lib, P=0) == _lib.DS_OK
+    assert lib.ds_greedy_lse(FAKE, 0, 10, FAKE, FAKE, FAKE, None) == _lib.DS_OK
+    assert lib.ds_greedy_lse(FAKE, 3, 0, FAKE, FAKE, FAKE, None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_greedy_lse(None, 3, 10, FAKE, FAKE, FAKE, None) == _lib.DS_ERR_INVALID_ARG
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(OSError):
+        saved = _lib._lib
+        _lib._lib = None
+        try:
+            _lib.load(str(tmp_path / "missing.so"))
+        finally:
+            _lib._lib = saved

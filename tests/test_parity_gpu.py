@@ -1,0 +1,329 @@
+"""GPU parity: libdsample (through the C ABI) against the CPU oracle, element by element.
+
+Bar (tokens): bit-exact, except cells whose two best perturbed scores (oracle, double) are
+within 1e-5 relative of each other; those near-ties are counted and reported, not failed.
+Bar (logprob, lse): |delta| <= 1e-4 absolute (fp32 accumulation on the GPU, double in the oracle).
+Bar (max, argmax, temperature-0 tokens): bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import vocab_wide_logit_gb300 as pkg
+from vocab_wide_logit_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+LOGPROB_TOL = 1e-4
+NEAR_TIE_REL = 1e-5
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkg.load()
+    return torch.device("cuda:0")
+
+
+class Dev:
+    """Device copies of one SampleInputs."""
+
+    def __init__(self, inp, dev):
+        self.inp = inp
+        self.rid = torch.from_numpy(inp.request_ids).to(dev)
+        self.sl = torch.from_numpy(inp.seq_lens.astype(np.int32)).to(dev)
+        self.g = torch.from_numpy(inp.guidance).to(dev)
+        self.tau = torch.from_numpy(inp.temperature).to(dev)
+        self.c = inp.c_logits.to(dev)
+        self.u = inp.u_logits.to(dev) if inp.u_logits is not None else None
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run(self, seed, iteration, c=None, u="same"):
+        c = self.c if c is None else c
+        u = self.u if isinstance(u, str) else u
+        tok = torch.full((self.inp.C, self.inp.P), -7, dtype=torch.int32, device=c.device)
+        lp = torch.full((self.inp.C, self.inp.P), 7.0, dtype=torch.float32, device=c.device)
+        pkg.ds_sample(self.rid, c, u, self.sl, self.g, self.tau, self.inp.top_ratio, seed, iteration, tok, lp,
+                      d_status=self.status, B=self.inp.B, C=self.inp.C, P=self.inp.P, V=self.inp.V)
+        torch.cuda.synchronize()
+        return tok.cpu().numpy().reshape(-1), lp.cpu().numpy().reshape(-1)
+
+
+def oracle_cells(inp, seed, iteration, cells=None):
+    return oracle.sample_cells(inp.request_ids, wl.bf16_bits(inp.c_logits),
+                               wl.bf16_bits(inp.u_logits) if inp.u_logits is not None else None,
+                               inp.seq_lens, inp.C, inp.P, inp.V, inp.guidance, inp.temperature,
+                               inp.top_ratio, seed, iteration, cells)
+
+
+def compare(inp, got_tok, got_lp, ref, cells=None, max_near_frac=0.01, label=""):
+    if cells is None:
+        cells = np.arange(inp.C * inp.P)
+    gt = got_tok[cells]
+    gl = got_lp[cells]
+    gap = ref["top1"] - ref["top2"]
+    near = np.abs(gap) < NEAR_TIE_REL * np.maximum(np.abs(ref["top1"]), 1.0)
+    match = gt == ref["tokens"]
+    bad = ~match & ~near
+    if bad.any():
+        j = np.nonzero(bad)[0][:10]
+        raise AssertionError("%s: %d token mismatches outside near-ties, e.g. cells %s gpu %s oracle %s "
+                             "top1 %s top2 %s" % (label, bad.sum(), cells[j], gt[j], ref["tokens"][j],
+                                                  ref["top1"][j], ref["top2"][j]))
+    d = np.abs(gl[match].astype(np.float64) - ref["logprobs"][match])
+    fin = np.isfinite(ref["logprobs"][match])
+    assert np.all(d[fin] <= LOGPROB_TOL), "%s: max |dlogprob| %g" % (label, d[fin].max())
+    assert np.all(np.isnan(gl[match][~fin]) == np.isnan(ref["logprobs"][match][~fin]))
+    # temperature-0 cells are exact argmaxes: no exemption
+    n_near_mismatch = int((~match & near).sum())
+    assert n_near_mismatch <= max(1, int(max_near_frac * len(cells))), "%s: %d near-tie mismatches" % (
+        label, n_near_mismatch)
+    return {"cells": len(cells), "near_ties": int(near.sum()), "near_tie_mismatches": n_near_mismatch,
+            "max_dlogprob": float(d[fin].max()) if fin.any() else 0.0}
+
+
+# ------------------------------------------------------------------------------------------ configs
+def test_config1_all_cells():
+    dev = _dev()
+    inp = wl.config1()
+    d = Dev(inp, dev)
+    tok, lp = d.run(inp.seed, 0)
+    ref = oracle_cells(inp, inp.seed, 0)
+    st = compare(inp, tok, lp, ref, label="cfg1")
+    assert int(d.status.item()) == 0
+    print("cfg1", st)
+
+
+def test_config2_mixed_guidance_and_temperature():
+    dev = _dev()
+    inp = wl.config2()
+    assert (inp.guidance == 0).any() and (inp.guidance != 0).any()
+    assert (inp.temperature == 0).any() and (inp.temperature != 0).any()
+    d = Dev(inp, dev)
+    for it in (0, 1, 5):
+        tok, lp = d.run(inp.seed, it)
+        ref = oracle_cells(inp, inp.seed, it)
+        st = compare(inp, tok, lp, ref, label="cfg2 it%d" % it)
+        # greedy requests: exact argmax everywhere
+        greedy_rows = np.repeat(inp.temperature == 0, inp.seq_lens)
+        gmask = np.tile(greedy_rows, inp.C)
+        assert np.array_equal(tok[gmask], ref["tokens"][gmask])
+    assert int(d.status.item()) == 0
+    print("cfg2", st)
+
+
+def test_config3_full_batch_sampled_cells():
+    """Full-size launch (as the benchmark times it); the oracle checks 3000 sampled cells
+    on each of four of the 32 iterations."""
+    dev = _dev()
+    inp = wl.config3()
+    d = Dev(inp, dev)
+    rng = np.random.Generator(np.random.PCG64(33))
+    for it in (0, 1, 17, 31):
+        tok, lp = d.run(inp.seed, it)
+        cells = np.sort(rng.choice(inp.C * inp.P, size=3000, replace=False))
+        ref = oracle_cells(inp, inp.seed, it, cells)
+        st = compare(inp, tok, lp, ref, cells, label="cfg3 it%d" % it)
+        assert (tok >= 0).all() and (tok < inp.V).all()
+        assert np.all(lp <= 1e-6)
+    assert int(d.status.item()) == 0
+    print("cfg3", st)
+
+
+def test_config4_greedy_large_vocab():
+    dev = _dev()
+    g = wl.config4()
+    x = g.logits.to(dev)
+    mx, lse, am = pkg.greedy_lse(x)
+    torch.cuda.synchronize()
+    ref = oracle.greedy_rows(wl.bf16_bits(g.logits), g.n, g.V)
+    assert np.array_equal(mx.cpu().numpy(), ref["max"])
+    assert np.array_equal(am.cpu().numpy(), ref["argmax"])
+    assert np.max(np.abs(lse.cpu().numpy() - ref["lse"])) <= LOGPROB_TOL
+    for row, ids in zip(g.planted_rows, g.planted_ids):
+        assert am[row].item() == ids.min()
+    p = np.exp(mx.cpu().numpy().astype(np.float64) - lse.cpu().numpy())
+    p_ref = np.exp(ref["max"].astype(np.float64) - ref["lse"])
+    assert np.max(np.abs(p - p_ref) / p_ref) <= 2e-4
+
+
+def test_config5_large_vocab_sampled_cells():
+    dev = _dev()
+    inp = wl.config5()
+    d = Dev(inp, dev)
+    tok, lp = d.run(inp.seed, 0)
+    rng = np.random.Generator(np.random.PCG64(55))
+    cells = np.sort(rng.choice(inp.C * inp.P, size=96, replace=False))
+    ref = oracle_cells(inp, inp.seed, 0, cells)
+    st = compare(inp, tok, lp, ref, cells, label="cfg5")
+    assert int(d.status.item()) == 0
+    print("cfg5", st)
+
+
+# ------------------------------------------------------------------------------------------ edge grids
+@pytest.mark.parametrize("V", [1, 2, 7, 8, 9, 33, 255, 1023, 1025, 2041, 2042, 4097, 20000, 70001])
+def test_vocab_grid(V):
+    dev = _dev()
+    inp = wl.make_sample_inputs("V%d" % V, C=3, seq_lens=[1, 4, 2, 3], V=V, guidance=[2.0, 0.0, 1.5, 0.5],
+                                temperature=[0.9, 0.0, 0.7, 2.0], sigma_c=3.0, sigma_u=1.0, top_ratio=0.1,
+                                seed=V)
+    d = Dev(inp, dev)
+    for it in (0, 3):
+        tok, lp = d.run(11 + V, it)
+        ref = oracle_cells(inp, 11 + V, it)
+        compare(inp, tok, lp, ref, label="V=%d it%d" % (V, it))
+    assert int(d.status.item()) == 0
+
+
+@pytest.mark.parametrize("ratio", [1e-6, 0.01, 0.1, 0.5, 0.97, 1.0])
+@pytest.mark.parametrize("V", [1025, 30011])
+def test_top_ratio_grid(ratio, V):
+    dev = _dev()
+    inp = wl.make_sample_inputs("ratio", C=2, seq_lens=[3, 2], V=V, guidance=[1.0, 0.0], temperature=[1.3, 0.8],
+                                sigma_c=2.0, sigma_u=1.0, top_ratio=ratio, seed=7)
+    d = Dev(inp, dev)
+    tok, lp = d.run(5, 2)
+    ref = oracle_cells(inp, 5, 2)
+    compare(inp, tok, lp, ref, label="ratio=%g V=%d" % (ratio, V))
+
+
+def test_unguided_batch_passes_no_u():
+    dev = _dev()
+    for V in (1025, 9000):
+        inp = wl.make_sample_inputs("nou", C=2, seq_lens=[5, 1, 6], V=V, guidance=[0.0, 0.0, 0.0],
+                                    temperature=[0.9, 0.0, 1.1], sigma_c=2.0, sigma_u=1.0, top_ratio=0.1, seed=3)
+        assert inp.u_logits is None
+        d = Dev(inp, dev)
+        tok, lp = d.run(9, 1)
+        compare(inp, tok, lp, oracle_cells(inp, 9, 1), label="no-u V=%d" % V)
+        assert int(d.status.item()) == 0
+
+
+def _planted(V, C, T, tie_at, k_ratio, seed):
+    """Rows where the logits hold many exact ties: at the maximum, and straddling the top-k cut."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    base = np.round(rng.standard_normal((C, T, V)) * 2.0 * 4) / 4  # quarter steps: plenty of equal values
+    return base.astype(np.float32)
+
+
+@pytest.mark.parametrize("V", [1025, 248320])
+def test_exact_ties_at_max_and_at_cut(V):
+    """Coarsely quantised logits: many ids share each value, so the k-th value is tied and the
+    kept set must take the smallest ids; the max is tied too (smallest id for temperature 0)."""
+    dev = _dev()
+    C, T = 1, 6
+    z = _planted(V, C, T, None, 0.1, 21)
+    c = wl.to_bf16(z)
+    inp = wl.SampleInputs(name="ties", C=C, V=V, seq_lens=np.array([T], np.int32),
+                          request_ids=np.array([77], np.int32), guidance=np.array([0.0], np.float32),
+                          temperature=np.array([0.6], np.float32), top_ratio=0.1, seed=1, c_logits=c,
+                          u_logits=None)
+    d = Dev(inp, dev)
+    ref = oracle_cells(inp, 1, 0)
+    assert (ref["thresh_ties"] > 0).all()
+    tok, lp = d.run(1, 0)
+    compare(inp, tok, lp, ref, label="ties V=%d" % V)
+    inp.temperature = np.array([0.0], np.float32)
+    d = Dev(inp, dev)
+    tok, lp = d.run(1, 0)
+    ref = oracle_cells(inp, 1, 0)
+    assert np.array_equal(tok, ref["tokens"])
+    assert np.array_equal(tok, ref["argmax"])
+
+
+def test_misaligned_rows_and_u_alignment_differing_from_c():
+    """Rows that start at arbitrary 2-byte offsets, with u's rows aligned differently from c's."""
+    dev = _dev()
+    for V in (1025, 5003):
+        inp = wl.make_sample_inputs("mis", C=2, seq_lens=[3, 4], V=V, guidance=[0.0, 2.0], temperature=[0.9, 0.9],
+                                    sigma_c=2.0, sigma_u=1.0, top_ratio=0.1, seed=4)
+        d = Dev(inp, dev)
+        cbuf = torch.zeros(inp.c_logits.numel() + 3, dtype=torch.bfloat16, device=dev)
+        cbuf[1:1 + inp.c_logits.numel()] = d.c.reshape(-1)
+        ubuf = torch.zeros(inp.u_logits.numel() + 7, dtype=torch.bfloat16, device=dev)
+        ubuf[6:6 + inp.u_logits.numel()] = d.u.reshape(-1)
+        c_view = cbuf[1:1 + inp.c_logits.numel()].view(inp.C, inp.P, V)
+        u_view = ubuf[6:6 + inp.u_logits.numel()].view(inp.C, inp.P_u, V)
+        tok, lp = d.run(8, 2, c=c_view, u=u_view)
+        compare(inp, tok, lp, oracle_cells(inp, 8, 2), label="misaligned V=%d" % V)
+
+
+def test_neg_inf_logits():
+    dev = _dev()
+    for V in (1025, 9000):
+        rng = np.random.Generator(np.random.PCG64(2))
+        z = (rng.standard_normal((1, 4, V)) * 2).astype(np.float32)
+        z[0, 0, :] = -np.inf                       # whole row -inf
+        z[0, 1, : V - 5] = -np.inf                 # fewer finite values than k
+        z[0, 2, ::2] = -np.inf                     # half masked
+        inp = wl.SampleInputs(name="inf", C=1, V=V, seq_lens=np.array([2, 2], np.int32),
+                              request_ids=np.array([5, 6], np.int32), guidance=np.array([0.0, 0.0], np.float32),
+                              temperature=np.array([0.9, 0.0], np.float32), top_ratio=0.1, seed=1,
+                              c_logits=wl.to_bf16(z), u_logits=None)
+        d = Dev(inp, dev)
+        tok, lp = d.run(3, 0)
+        ref = oracle_cells(inp, 3, 0)
+        compare(inp, tok, lp, ref, label="inf V=%d" % V)
+        assert tok[0] == 0 and np.isnan(lp[0])
+
+
+def test_repeat_calls_are_deterministic():
+    dev = _dev()
+    inp = wl.config2()
+    d = Dev(inp, dev)
+    a = d.run(42, 9)
+    b = d.run(42, 9)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_device_side_layout_errors_are_reported():
+    dev = _dev()
+    inp = wl.make_sample_inputs("err", C=1, seq_lens=[3, 3], V=1025, guidance=[1.0, 0.0], temperature=[0.5, -1.0],
+                                sigma_c=1.0, sigma_u=1.0, top_ratio=0.1, seed=1)
+    d = Dev(inp, dev)
+    tok, lp = d.run(1, 0)
+    assert int(d.status.item()) & pkg.DS_DEV_ERR_PARAM
+    assert (tok[3:] == -1).all() and np.isnan(lp[3:]).all()
+    assert (tok[:3] >= 0).all()
+    # guided request but no u
+    d.status.zero_()
+    tok, lp = d.run(1, 0, u=None)
+    assert int(d.status.item()) & pkg.DS_DEV_ERR_NO_UNCOND
+    # seq_lens that do not sum to P
+    d.status.zero_()
+    d.sl.copy_(torch.tensor([3, 2], dtype=torch.int32))
+    tok, lp = d.run(1, 0)
+    assert int(d.status.item()) & pkg.DS_DEV_ERR_LAYOUT
+    assert (tok == -1).all()
+
+
+def test_greedy_edge_sizes():
+    dev = _dev()
+    for V in (1, 7, 1025, 32769, 248321):
+        g = wl.make_greedy_inputs("gv", n=5, V=V, sigma=3.0, seed=V, tie_fraction=0.4)
+        x = g.logits.to(dev)
+        mx, lse, am = pkg.greedy_lse(x)
+        torch.cuda.synchronize()
+        ref = oracle.greedy_rows(wl.bf16_bits(g.logits), g.n, g.V)
+        assert np.array_equal(am.cpu().numpy(), ref["argmax"]), V
+        assert np.array_equal(mx.cpu().numpy(), ref["max"]), V
+        assert np.max(np.abs(lse.cpu().numpy() - ref["lse"])) <= LOGPROB_TOL
+    # odd start address
+    g = wl.make_greedy_inputs("odd", n=3, V=1001, sigma=3.0, seed=1)
+    buf = torch.zeros(g.logits.numel() + 1, dtype=torch.bfloat16, device=dev)
+    buf[1:] = g.logits.reshape(-1).to(dev)
+    mx, lse, am = pkg.greedy_lse(buf[1:].view(3, 1001))
+    torch.cuda.synchronize()
+    ref = oracle.greedy_rows(wl.bf16_bits(g.logits), g.n, g.V)
+    assert np.array_equal(am.cpu().numpy(), ref["argmax"])
+
+
+def test_empty_calls_launch_nothing():
+    dev = _dev()
+    e = torch.empty(0, dtype=torch.int32, device=dev)
+    f = torch.empty(0, dtype=torch.float32, device=dev)
+    c = torch.empty((2, 0, 1025), dtype=torch.bfloat16, device=dev)
+    assert pkg.ds_sample(e, c, None, e, f, f, 0.1, 0, 0, e, f, B=0, C=2, P=0, V=1025) == 0
+    x = torch.empty((0, 100), dtype=torch.bfloat16, device=dev)
+    assert pkg.ds_greedy_lse(x, f, f, e) == 0

@@ -1,0 +1,102 @@
+"""ctypes binding of libdsample (argument marshalling only).
+
+Every step of the sampling and greedy passes runs in the CUDA library; this
+module only turns torch tensors into device pointers and the current CUDA
+stream into a handle. There is no fallback: if the library is missing the
+import of a call raises.
+"""
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libdsample.so")
+
+DS_OK = 0
+DS_ERR_INVALID_ARG = 1
+DS_ERR_UNSUPPORTED = 2
+DS_ERR_CUDA = 3
+DS_DEV_ERR_LAYOUT = 1
+DS_DEV_ERR_NO_UNCOND = 2
+DS_DEV_ERR_PARAM = 4
+DS_MAX_VOCAB = 262137
+
+EXPORTED = ("ds_sample", "ds_greedy_lse", "ds_status_string", "ds_top_k")
+
+_lib = None
+
+
+class DsError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (fn, status_string(code), code))
+
+
+def load(path: str = LIB_PATH):
+    """Load libdsample.so (raises OSError when it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise OSError("libdsample.so not built at %s: run __graft_entry__.build() or "
+                      "python vocab_wide_logit_gb300/build.py" % path)
+    L = ctypes.CDLL(path)
+    vp, i32, u32, u64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_float
+    L.ds_sample.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, f32, u64, u32, vp, vp, vp, vp]
+    L.ds_sample.restype = ctypes.c_int
+    L.ds_greedy_lse.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+    L.ds_greedy_lse.restype = ctypes.c_int
+    L.ds_status_string.argtypes = [ctypes.c_int]
+    L.ds_status_string.restype = ctypes.c_char_p
+    L.ds_top_k.argtypes = [f32, i32]
+    L.ds_top_k.restype = i32
+    _lib = L
+    return L
+
+
+def status_string(code: int) -> str:
+    return load().ds_status_string(int(code)).decode()
+
+
+def top_k(top_ratio: float, V: int) -> int:
+    return int(load().ds_top_k(float(top_ratio), int(V)))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def ds_sample(request_ids, c_logits, u_logits, seq_lens, guidance, temperature, top_ratio, seed,
+              iteration, out_tokens, out_logprobs, d_status=None, B=None, C=None, P=None, V=None,
+              stream=None, check=True):
+    """Call ds_sample on device tensors. Shapes: c_logits [C, P, V] bf16, u_logits [C, P_u, V]
+    bf16 or None, request_ids/seq_lens int32 [B], guidance/temperature float32 [B],
+    out_tokens int32 [C, P], out_logprobs float32 [C, P], d_status uint32/int32 [1] or None."""
+    if C is None:
+        C, P, V = c_logits.shape
+    if B is None:
+        B = seq_lens.shape[0]
+    rc = load().ds_sample(_ptr(request_ids), _ptr(c_logits), _ptr(u_logits), _ptr(seq_lens), int(B),
+                          int(C), int(P), int(V), _ptr(guidance), _ptr(temperature), float(top_ratio),
+                          int(seed) & (2 ** 64 - 1), int(iteration), _ptr(out_tokens), _ptr(out_logprobs),
+                          _ptr(d_status), _stream(stream))
+    if check and rc != DS_OK:
+        raise DsError("ds_sample", rc)
+    return rc
+
+
+def ds_greedy_lse(logits, out_max, out_lse, out_argmax, n=None, V=None, stream=None, check=True):
+    """Call ds_greedy_lse on device tensors: logits [n, V] bf16, outputs [n] float32/float32/int32."""
+    if n is None:
+        n, V = logits.shape
+    rc = load().ds_greedy_lse(_ptr(logits), int(n), int(V), _ptr(out_max), _ptr(out_lse), _ptr(out_argmax),
+                              _stream(stream))
+    if check and rc != DS_OK:
+        raise DsError("ds_greedy_lse", rc)
+    return rc

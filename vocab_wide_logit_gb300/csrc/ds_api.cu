@@ -1,0 +1,137 @@
+// ds_api.cu -- the C ABI of libdsample: argument checks, launch parameters, dispatch.
+//
+// Host work per call is O(1): validate the scalars, derive the kept count k
+// and the two normal quantiles that seed the kernels' threshold guesses, pick
+// the kernel by vocabulary size, and launch asynchronously on the caller's
+// stream. Nothing is allocated and nothing is synchronised.
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dsample.h"
+#include "ds_launch.h"
+
+namespace {
+
+// Upper-tail standard normal quantile: x with P(N(0,1) > x) = p, by bisection on
+// erfc (host-side, double). p <= 0 -> +inf, p >= 1 -> -inf.
+double normal_upper_quantile(double p) {
+  if (p <= 0.0) return INFINITY;
+  if (p >= 1.0) return -INFINITY;
+  double lo = -40.0, hi = 40.0;
+  for (int it = 0; it < 200; ++it) {
+    const double mid = 0.5 * (lo + hi);
+    const double tail = 0.5 * std::erfc(mid / std::sqrt(2.0));
+    if (tail > p)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return 0.5 * (lo + hi);
+}
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  static int cached_dev = -1, cached_sms = 0;
+  if (dev != cached_dev) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cached_dev = dev;
+    cached_sms = sms;
+  }
+  return cached_sms;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ds_status_string(ds_status s) {
+  switch (s) {
+    case DS_OK: return "ok";
+    case DS_ERR_INVALID_ARG: return "invalid argument";
+    case DS_ERR_UNSUPPORTED: return "unsupported size for this build";
+    case DS_ERR_CUDA: return "CUDA launch or runtime error";
+  }
+  return "unknown status";
+}
+
+int32_t ds_top_k(float top_ratio, int32_t V) {
+  if (V < 1 || !(top_ratio > 0.0f) || !(top_ratio <= 1.0f)) return 0;
+  const float prod = top_ratio * (float)V;  // fp32 product, as the contract states
+  long long k = (long long)ceilf(prod);
+  if (k < 1) k = 1;
+  if (k > V) k = V;
+  return (int32_t)k;
+}
+
+ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void* u_logits,
+                    const int32_t* seq_lens, int32_t B, int32_t C, int32_t P, int32_t V,
+                    const float* guidance, const float* temperature, float top_ratio,
+                    uint64_t seed, uint32_t iteration, int32_t* out_tokens, float* out_logprobs,
+                    uint32_t* d_status, void* stream) {
+  if (B < 0 || C < 0 || P < 0 || V < 1) return DS_ERR_INVALID_ARG;
+  if (C > DS_MAX_ROWS) return DS_ERR_INVALID_ARG;
+  if (iteration > DS_MAX_ITERATION) return DS_ERR_INVALID_ARG;
+  if (!(top_ratio > 0.0f) || !(top_ratio <= 1.0f)) return DS_ERR_INVALID_ARG;
+  if (C == 0 || P == 0) return DS_OK;
+  if (B == 0) return DS_ERR_INVALID_ARG;  // P > 0 positions need an owner
+  if (!request_ids || !c_logits || !seq_lens || !guidance || !temperature || !out_tokens || !out_logprobs)
+    return DS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(c_logits) & 1) || (reinterpret_cast<uintptr_t>(u_logits) & 1))
+    return DS_ERR_INVALID_ARG;
+  if (V > DS_MAX_VOCAB || V > ds::cluster_kernel_max_vocab()) return DS_ERR_UNSUPPORTED;
+  if ((long long)C * (long long)P * (long long)V > (1LL << 46)) return DS_ERR_UNSUPPORTED;
+
+  ds::SampleArgs a;
+  a.request_ids = request_ids;
+  a.c = static_cast<const uint16_t*>(c_logits);
+  a.u = static_cast<const uint16_t*>(u_logits);
+  a.seq_lens = seq_lens;
+  a.guidance = guidance;
+  a.temperature = temperature;
+  a.out_tokens = out_tokens;
+  a.out_logprobs = out_logprobs;
+  a.d_status = d_status;
+  a.B = B;
+  a.C = C;
+  a.P = P;
+  a.V = V;
+  a.k = ds_top_k(top_ratio, V);
+  // Threshold guesses: aim the candidate count a little above k so that the
+  // verified count rarely falls short, and the upper count a little below.
+  const double kk = (double)a.k;
+  const double spread = 1.5 * std::sqrt(kk * (1.0 - kk / (double)V)) + 0.02 * kk + 4.0;
+  const double target_lo = kk + spread;
+  const double target_hi = kk - spread;
+  a.q_lo = (target_lo >= (double)V) ? -INFINITY : (float)normal_upper_quantile(target_lo / (double)V);
+  a.q_hi = (target_hi < 1.0) ? INFINITY : (float)normal_upper_quantile(target_hi / (double)V);
+  a.key0 = (uint32_t)(seed & 0xffffffffull);
+  a.key1 = (uint32_t)(seed >> 32);
+  a.iter_hi = iteration << 8;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (V <= ds::warp_kernel_max_vocab()) {
+    const int sms = device_sm_count();
+    if (sms <= 0) return DS_ERR_CUDA;
+    e = ds::launch_sample_warp(a, st, sms);
+  } else {
+    e = ds::launch_sample_cluster(a, st);
+  }
+  return e == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+ds_status ds_greedy_lse(const void* logits, int32_t n, int32_t V, float* out_max, float* out_lse,
+                        int32_t* out_argmax, void* stream) {
+  if (n < 0 || V < 1) return DS_ERR_INVALID_ARG;
+  if (n == 0) return DS_OK;
+  if (!logits || !out_max || !out_lse || !out_argmax) return DS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) & 1) return DS_ERR_INVALID_ARG;
+  const cudaError_t e = ds::launch_greedy(static_cast<const uint16_t*>(logits), n, V, out_max, out_lse,
+                                          out_argmax, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// ds_sample_common.cuh -- pieces of the sampling pass shared by the warp and cluster kernels.
+#pragma once
+
+#include "ds_device.cuh"
+#include "gumbel_bounds.inc"
+
+namespace ds {
+
+// Position -> request mapping of the packed layout ("Add a sampler resource for
+// discrete diffusion", Contract: [rows, positions, vocab] packed across
+// requests; guidance 0 builds no unconditional document, so u packs only the
+// guided requests).
+struct ReqCursor {
+  int32_t r;       // request index
+  int32_t off;     // first position of request r
+  int32_t T;       // seq_lens[r]
+  int32_t off_u;   // first row of request r inside u's packed positions
+  float g, tau;
+  uint32_t rid;
+};
+
+// Whole-batch totals, computed by each warp (O(B / 32)).
+struct BatchTotals {
+  long long tot;    // sum of seq_lens
+  long long tot_u;  // sum over guided requests
+  bool bad;         // a negative seq_len
+};
+
+__device__ __forceinline__ BatchTotals warp_batch_totals(const SampleArgs& a, int lane) {
+  BatchTotals bt{0, 0, false};
+  for (int base = 0; base < a.B; base += 32) {
+    const int r = base + lane;
+    int T = 0;
+    float g = 0.f;
+    if (r < a.B) {
+      T = a.seq_lens[r];
+      g = a.guidance[r];
+    }
+    const bool neg = T < 0;
+    bt.bad |= __any_sync(0xffffffffu, neg);
+    const int Tc = neg ? 0 : T;
+    bt.tot += warp_sum_i(Tc);
+    bt.tot_u += warp_sum_i(g != 0.f ? Tc : 0);
+  }
+  return bt;
+}
+
+// Find the request that owns position p by a warp-parallel scan from request 0.
+// Returns false when no request owns p.
+__device__ __forceinline__ bool warp_find_request(const SampleArgs& a, int p, int lane, ReqCursor& cur) {
+  int off = 0, off_u = 0;
+  for (int base = 0; base < a.B; base += 32) {
+    const int r = base + lane;
+    int T = 0;
+    float g = 0.f;
+    if (r < a.B) {
+      T = max(a.seq_lens[r], 0);
+      g = a.guidance[r];
+    }
+    const int Tu = (g != 0.f) ? T : 0;
+    const int ex = warp_excl_scan(T, lane);
+    const int exu = warp_excl_scan(Tu, lane);
+    const bool own = (r < a.B) && (p >= off + ex) && (p < off + ex + T);
+    const unsigned m = __ballot_sync(0xffffffffu, own);
+    if (m) {
+      const int src = __ffs(m) - 1;
+      cur.r = base + src;
+      cur.off = off + __shfl_sync(0xffffffffu, ex, src);
+      cur.T = __shfl_sync(0xffffffffu, T, src);
+      cur.off_u = off_u + __shfl_sync(0xffffffffu, exu, src);
+      cur.g = a.guidance[cur.r];
+      cur.tau = a.temperature[cur.r];
+      cur.rid = (uint32_t)a.request_ids[cur.r];
+      return true;
+    }
+    off += warp_sum_i(T);
+    off_u += warp_sum_i(Tu);
+  }
+  return false;
+}
+
+// Gumbel bounds of one Philox word.
+__device__ __forceinline__ float2 gumbel_bounds(uint32_t x) {
+  return __ldg(&kGumbelBounds[x >> DS_GUMBEL_BUCKET_SHIFT]);
+}
+
+// 64-bit composite key of (z, id): larger key = earlier in the order (z desc, id asc).
+__device__ __forceinline__ unsigned long long rank_key(float z, int id) {
+  return ((unsigned long long)order_key(z) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)id);
+}
+
+}  // namespace ds

@@ -1,7 +1,8 @@
 """Seeded synthetic inputs for the sampling pass and the greedy pass.
 
-This module only draws random inputs (numpy PCG64 streams, rounded to bf16 by
-torch): it holds none of the method's arithmetic. The tests feed the same
+This module only draws random inputs (torch CPU generators for the large normal
+draws, numpy PCG64 for small choices; values rounded to bf16 by torch): it
+holds none of the method's arithmetic. The tests feed the same
 inputs to the CUDA library and to the CPU oracle, and the benchmark times the
 library on them.
 
@@ -80,23 +81,26 @@ def make_sample_inputs(name, C, seq_lens, V, guidance, temperature, sigma_c, sig
     temperature = np.asarray(temperature, dtype=np.float32)
     B = int(seq_lens.shape[0])
     P = int(seq_lens.sum())
-    rng = np.random.Generator(np.random.PCG64(seed if gen_seed is None else gen_seed))
-    c32 = rng.standard_normal((C, P, V), dtype=np.float32)
-    c32 *= np.float32(sigma_c)
-    c = to_bf16(c32)
+    gen = torch.Generator().manual_seed(int(seed if gen_seed is None else gen_seed))
+    c32 = torch.randn((C, P, V), generator=gen, dtype=torch.float32)
+    c32 *= float(np.float32(sigma_c))
+    c = c32.to(torch.bfloat16)
     del c32
     guided = guidance != 0
     u = None
     if guided.any():
-        # Positions of guided requests, in request order.
-        offs = np.concatenate([[0], np.cumsum(seq_lens)]).astype(np.int64)
-        pos = np.concatenate([np.arange(offs[r], offs[r + 1]) for r in range(B) if guided[r]])
-        cu = c[:, torch.from_numpy(pos)].float().numpy()
-        noise = rng.standard_normal(cu.shape, dtype=np.float32)
-        noise *= np.float32(sigma_u)
+        if guided.all():
+            cu = c.float()
+        else:
+            # Positions of guided requests, in request order.
+            offs = np.concatenate([[0], np.cumsum(seq_lens)]).astype(np.int64)
+            pos = np.concatenate([np.arange(offs[r], offs[r + 1]) for r in range(B) if guided[r]])
+            cu = c[:, torch.from_numpy(pos)].float()
+        noise = torch.randn(cu.shape, generator=gen, dtype=torch.float32)
+        noise *= float(np.float32(sigma_u))
         cu += noise
         del noise
-        u = to_bf16(cu)
+        u = cu.to(torch.bfloat16)
         del cu
     rids = np.array([request_id_of(r) for r in range(B)], dtype=np.int32)
     return SampleInputs(name=name, C=C, V=V, seq_lens=seq_lens, request_ids=rids,
@@ -165,9 +169,9 @@ def make_greedy_inputs(name, n, V, sigma, seed, tie_fraction=0.25, tie_spread_ro
     the row maximum is written at 2-4 seeded random ids, so the row's argmax is a planted tie
     (expect the smallest id). One planted row puts its ids far apart along the row."""
     rng = np.random.Generator(np.random.PCG64(seed))
-    x = rng.standard_normal((n, V), dtype=np.float32)
-    x *= np.float32(sigma)
-    t = to_bf16(x)
+    x = torch.randn((n, V), generator=torch.Generator().manual_seed(int(seed)), dtype=torch.float32)
+    x *= float(np.float32(sigma))
+    t = x.to(torch.bfloat16)
     del x
     bits = t.view(torch.int16)
     n_planted = int(round(tie_fraction * n))

@@ -178,8 +178,8 @@ def make_greedy_inputs(name, n, V, sigma, seed, tie_fraction=0.25, tie_spread_ro
     rows = np.sort(rng.choice(n, size=n_planted, replace=False)) if n_planted else np.zeros(0, np.int64)
     planted_ids = []
     for j, r in enumerate(rows):
-        cnt = int(rng.integers(2, 5))
-        if tie_spread_row and j == 0 and V >= 16:
+        cnt = min(int(rng.integers(2, 5)), V)
+        if tie_spread_row and j == 0 and V >= 16 and cnt >= 2:
             ids = np.array([3, V // 2 + 1, V - 2][:cnt] if cnt <= 3 else [3, V // 3, (2 * V) // 3, V - 2])
         else:
             ids = np.sort(rng.choice(V, size=cnt, replace=False))

@@ -51,6 +51,12 @@ __device__ __forceinline__ Triple warp_merge(Triple t) {
   return t;
 }
 
+__device__ __forceinline__ float max3g(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 template <int NT, int UNROLL>
 __global__ void __launch_bounds__(NT) k_greedy_lse(const uint16_t* __restrict__ x, int n, int V,
                                                   float* __restrict__ out_max, float* __restrict__ out_lse,
@@ -61,6 +67,7 @@ __global__ void __launch_bounds__(NT) k_greedy_lse(const uint16_t* __restrict__ 
   const int cs = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const float2 l2e = make_float2(kLog2e, kLog2e);
 
   for (int row = blockIdx.y; row < n; row += gridDim.y) {
     const uint16_t* xr = x + (long long)row * V;
@@ -79,35 +86,51 @@ __global__ void __launch_bounds__(NT) k_greedy_lse(const uint16_t* __restrict__ 
         const int q = q0 + u * NT;
         v[u] = (q < q_hi) ? ld_stream16(base + q) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
       }
+      float2 f[UNROLL][4];
+      float bm = -kInf;
 #pragma unroll
       for (int u = 0; u < UNROLL; ++u) {
-        const int q = q0 + u * NT;
-        float f[8];
-        unpack8(v[u], f);
-        if (q == 0 || q >= nq - 1) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int id = 8 * q - dc + e;
-            if (id < 0 || id >= V) f[e] = -kInf;
+        for (int i = 0; i < 4; ++i) f[u][i] = make_float2(bf_lo(w[i]), bf_hi(w[i]));
+        const int q = q0 + u * NT;
+        if (q == 0 || q >= nq - 1) {  // row edges: mask the ids outside [0, V)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int id = 8 * q - dc + 2 * i;
+            if (id < 0 || id >= V) f[u][i].x = -kInf;
+            if (id + 1 < 0 || id + 1 >= V) f[u][i].y = -kInf;
           }
         }
-        float cm = f[0];
 #pragma unroll
-        for (int e = 1; e < 8; ++e) cm = fmaxf(cm, f[e]);
-        if (cm > t.m) {
-          t.s = (t.m == -kInf) ? 0.f : t.s * ex2_approx((t.m - cm) * kLog2e);
-          t.m = cm;
-          int a = INT_MAX;
+        for (int i = 0; i < 4; ++i) bm = max3g(bm, f[u][i].x, f[u][i].y);
+      }
+      if (bm > t.m) {
+        // new running max: rescale the sum and take the first id attaining it
+        t.s = (t.m == -kInf) ? 0.f : t.s * ex2_approx((t.m - bm) * kLog2e);
+        t.m = bm;
+        int a = INT_MAX;
 #pragma unroll
-          for (int e = 7; e >= 0; --e)
-            if (f[e] == cm) a = 8 * q - dc + e;
-          t.a = a;
-        }
-        if (t.m != -kInf) {
-          const float mb = t.m * kLog2e;
+        for (int u = UNROLL - 1; u >= 0; --u)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) t.s += ex2_approx(fmaf(f[e], kLog2e, -mb));
-        }
+          for (int i = 3; i >= 0; --i) {
+            const int id = 8 * (q0 + u * NT) - dc + 2 * i;
+            if (f[u][i].y == bm) a = id + 1;
+            if (f[u][i].x == bm) a = id;
+          }
+        t.a = a;
+      }
+      if (t.m != -kInf) {
+        const float2 nml = make_float2(-t.m * kLog2e, -t.m * kLog2e);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 tt = __ffma2_rn(f[u][i], l2e, nml);
+            acc = __fadd2_rn(acc, make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
+          }
+        t.s += acc.x + acc.y;
       }
     }
     // block merge
@@ -138,11 +161,25 @@ __global__ void __launch_bounds__(NT) k_greedy_lse(const uint16_t* __restrict__ 
 // ---------------------------------------------------------------- launcher
 cudaError_t launch_greedy(const uint16_t* x, int n, int V, float* out_max, float* out_lse, int* out_argmax,
                           cudaStream_t st) {
-  constexpr int NT = 512;
+  constexpr int NT = 256;
   constexpr int UNROLL = 4;
-  // Slice of about 32K elements per CTA, cluster of up to 8 CTAs per row.
-  int cs = 1;
-  while (cs < 8 && (long long)V > 32768LL * cs) cs *= 2;
+  auto kern = k_greedy_lse<NT, UNROLL>;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, 0);
+  if (e != cudaSuccess) return e;
+  // Split each row over a cluster of cs CTAs so that all rows' CTAs fit in one
+  // wave when they can (no tail wave), with at least one 16-byte chunk per
+  // thread and at most 8 CTAs per row.
+  const long long slots = (long long)sms * (per_sm > 0 ? per_sm : 1);
+  const int nq = (V + 14) >> 3;
+  long long cs = slots / (n > 0 ? n : 1);
+  if (cs > 8) cs = 8;
+  if (cs > (nq + NT - 1) / NT) cs = (nq + NT - 1) / NT;
+  if (cs < 1) cs = 1;
   const int rows_grid = n < 65535 ? n : 65535;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)cs, (unsigned)rows_grid, 1);
@@ -156,7 +193,7 @@ cudaError_t launch_greedy(const uint16_t* x, int n, int V, float* out_max, float
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_greedy_lse<NT, UNROLL>, x, n, V, out_max, out_lse, out_argmax);
+  e = cudaLaunchKernelEx(&cfg, kern, x, n, V, out_max, out_lse, out_argmax);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -14,6 +14,7 @@
 // All branching that surrounds a cluster barrier depends only on values every
 // CTA of the cluster holds identically (per-request scalars and gathered
 // totals combined in rank order), so every CTA reaches every barrier.
+#include <cfloat>
 #include <climits>
 #include <cooperative_groups.h>
 
@@ -87,30 +88,123 @@ struct BlockRed {
   int i[NT / 32][4];
 };
 
-// Block-wide sums / max / min of up to 4 floats and 4 ints; result valid in every thread.
-// Float slots: op 0 = sum, 1 = max. Int slots: op 0 = sum, 1 = min.
+struct ClusterXchg {
+  Rec slot[2];  // this CTA's published record, alternating between rounds
+  Rec comb;     // the cluster-wide result of the last round
+  Top2 ctop;    // cluster-wide top-2 of the last Gumbel round
+  float cS;     // cluster-wide max lower score of the last Gumbel round
+};
+
+enum { OP_SUM = 0, OP_MAX = 1, OP_MIN = 1 };
+
+__device__ __forceinline__ float fred(float x, int op) { return op ? warp_max(x) : warp_sum(x); }
+__device__ __forceinline__ int ired(int x, int op) { return op ? warp_min_i(x) : warp_sum_i(x); }
+
+// Cluster-wide all-reduce of up to 4 floats (sum or max) and 4 ints (sum or
+// min): warp shuffles, then warp 0 over the CTA's warps, then warp 0 over the
+// cluster's CTAs (lane r reads CTA r's record through distributed shared
+// memory). Every CTA combines the same records in the same order, so every CTA
+// ends with bit-identical results, which all its threads read back.
 template <int NT>
-__device__ __forceinline__ void block_reduce(BlockRed<NT>& sm, float (&f)[4], const int (&fop)[4], int nf,
-                                             int (&v)[4], const int (&iop)[4], int ni) {
+__device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cl, ClusterXchg& xs, BlockRed<NT>& red,
+                                                  float (&f)[4], const int (&fop)[4], int nf, int (&v)[4],
+                                                  const int (&iop)[4], int ni, int& parity, int cs) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int j = 0; j < nf; ++j) f[j] = fop[j] ? warp_max(f[j]) : warp_sum(f[j]);
-  for (int j = 0; j < ni; ++j) v[j] = iop[j] ? warp_min_i(v[j]) : warp_sum_i(v[j]);
+  for (int j = 0; j < nf; ++j) f[j] = fred(f[j], fop[j]);
+  for (int j = 0; j < ni; ++j) v[j] = ired(v[j], iop[j]);
+  __syncthreads();  // the previous round's readers of red / comb are done
+  if (lane == 0) {
+    for (int j = 0; j < nf; ++j) red.f[wid][j] = f[j];
+    for (int j = 0; j < ni; ++j) red.i[wid][j] = v[j];
+  }
+  __syncthreads();
+  if (wid == 0) {
+    Rec r;
+    for (int j = 0; j < nf; ++j) {
+      const float x = (lane < NT / 32) ? red.f[lane][j] : (fop[j] ? -kInf : 0.f);
+      r.f[j] = fred(x, fop[j]);
+    }
+    for (int j = 0; j < ni; ++j) {
+      const int x = (lane < NT / 32) ? red.i[lane][j] : (iop[j] ? INT_MAX : 0);
+      r.i[j] = ired(x, iop[j]);
+    }
+    if (lane == 0) xs.slot[parity] = r;
+  }
+  cl.sync();
+  if (wid == 0) {
+    const Rec* src = cl.map_shared_rank(&xs.slot[parity], lane < cs ? lane : 0);
+    Rec r;
+    for (int j = 0; j < nf; ++j) {
+      const float x = (lane < cs) ? src->f[j] : (fop[j] ? -kInf : 0.f);
+      r.f[j] = fred(x, fop[j]);
+    }
+    for (int j = 0; j < ni; ++j) {
+      const int x = (lane < cs) ? src->i[j] : (iop[j] ? INT_MAX : 0);
+      r.i[j] = ired(x, iop[j]);
+    }
+    if (lane == 0) xs.comb = r;
+  }
+  __syncthreads();
+  for (int j = 0; j < nf; ++j) f[j] = xs.comb.f[j];
+  for (int j = 0; j < ni; ++j) v[j] = xs.comb.i[j];
+  parity ^= 1;
+}
+
+// Cluster-wide sum of one int.
+template <int NT>
+__device__ __forceinline__ int cluster_sum(cg::cluster_group& cl, ClusterXchg& xs, BlockRed<NT>& red, int x,
+                                           int& parity, int cs) {
+  float f[4] = {0.f, 0.f, 0.f, 0.f};
+  const int fop[4] = {0, 0, 0, 0};
+  int v[4] = {x, 0, 0, 0};
+  const int iop[4] = {0, 0, 0, 0};
+  cluster_allreduce<NT>(cl, xs, red, f, fop, 0, v, iop, 1, parity, cs);
+  return v[0];
+}
+
+// Cluster-wide argmax of (score desc, id asc) carrying z.
+template <int NT>
+__device__ __forceinline__ void cluster_argmax(cg::cluster_group& cl, ClusterXchg& xs, BlockRed<NT>& red,
+                                               float score, int id, float z, float& out_z, int& out_id,
+                                               int& parity, int cs) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int wl = warp_argmax_lane(score, id);
+  float s = __shfl_sync(0xffffffffu, score, wl);
+  int i = __shfl_sync(0xffffffffu, id, wl);
+  float zz = __shfl_sync(0xffffffffu, z, wl);
   __syncthreads();
   if (lane == 0) {
-    for (int j = 0; j < nf; ++j) sm.f[wid][j] = f[j];
-    for (int j = 0; j < ni; ++j) sm.i[wid][j] = v[j];
+    red.f[wid][0] = s; red.f[wid][1] = zz; red.i[wid][0] = i;
   }
   __syncthreads();
-  for (int j = 0; j < nf; ++j) {
-    float r = sm.f[0][j];
-    for (int w = 1; w < NT / 32; ++w) r = fop[j] ? fmaxf(r, sm.f[w][j]) : r + sm.f[w][j];
-    f[j] = r;
+  if (wid == 0) {
+    s = (lane < NT / 32) ? red.f[lane][0] : -kInf;
+    zz = (lane < NT / 32) ? red.f[lane][1] : 0.f;
+    i = (lane < NT / 32) ? red.i[lane][0] : INT_MAX;
+    wl = warp_argmax_lane(s, i);
+    Rec r;
+    r.f[0] = __shfl_sync(0xffffffffu, s, wl);
+    r.f[1] = __shfl_sync(0xffffffffu, zz, wl);
+    r.i[0] = __shfl_sync(0xffffffffu, i, wl);
+    if (lane == 0) xs.slot[parity] = r;
   }
-  for (int j = 0; j < ni; ++j) {
-    int r = sm.i[0][j];
-    for (int w = 1; w < NT / 32; ++w) r = iop[j] ? min(r, sm.i[w][j]) : r + sm.i[w][j];
-    v[j] = r;
+  cl.sync();
+  if (wid == 0) {
+    const Rec* src = cl.map_shared_rank(&xs.slot[parity], lane < cs ? lane : 0);
+    s = (lane < cs) ? src->f[0] : -kInf;
+    zz = (lane < cs) ? src->f[1] : 0.f;
+    i = (lane < cs) ? src->i[0] : INT_MAX;
+    wl = warp_argmax_lane(s, i);
+    Rec r;
+    r.f[0] = __shfl_sync(0xffffffffu, s, wl);
+    r.f[1] = __shfl_sync(0xffffffffu, zz, wl);
+    r.i[0] = __shfl_sync(0xffffffffu, i, wl);
+    if (lane == 0) xs.comb = r;
   }
+  __syncthreads();
+  out_z = xs.comb.f[1];
+  out_id = xs.comb.i[0];
+  parity ^= 1;
 }
 
 // Exclusive block scan of one int per thread; returns the prefix, writes the total.
@@ -122,28 +216,20 @@ __device__ __forceinline__ int block_excl_scan(int* wsum, int v, int& total) {
   if (lane == 31) wsum[wid] = ex + v;
   __syncthreads();
   int base = 0, tot = 0;
+#pragma unroll
   for (int w = 0; w < NT / 32; ++w) {
-    const int s = wsum[w];
-    if (w < wid) base += s;
-    tot += s;
+    const int s2 = wsum[w];
+    if (w < wid) base += s2;
+    tot += s2;
   }
   total = tot;
   return base + ex;
 }
 
-struct ClusterXchg {
-  Rec slot[2];
-  Rec peers[16];
-};
-
-// Publish thread 0's record and gather every CTA's record (rank order) into xs.peers.
-__device__ __forceinline__ void cluster_gather(cg::cluster_group& cl, ClusterXchg& xs, const Rec& mine,
-                                               int& parity, int cs) {
-  if (threadIdx.x == 0) xs.slot[parity] = mine;
-  cl.sync();
-  if ((int)threadIdx.x < cs) xs.peers[threadIdx.x] = *cl.map_shared_rank(&xs.slot[parity], (int)threadIdx.x);
-  __syncthreads();
-  parity ^= 1;
+__device__ __forceinline__ float max3c(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 template <int NT, int UNROLL>
@@ -167,6 +253,8 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
   const long long n_clusters = (long long)gridDim.x / cs;
   const long long cluster_id = (long long)blockIdx.x / cs;
   const int P = a.P, V = a.V, k = a.k;
+  const float2 neg1 = make_float2(-1.f, -1.f);
+  const float2 l2e = make_float2(kLog2e, kLog2e);
   int parity = 0;
 
   if (wid == 0) {
@@ -178,14 +266,12 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
   }
   __syncthreads();
   if (s_bad) {
-    if (rank == 0) {
+    if (rank == 0 && tid == 0) {
       for (long long cell = cluster_id; cell < n_cells; cell += n_clusters) {
-        if (tid == 0) {
-          a.out_tokens[cell] = -1;
-          a.out_logprobs[cell] = __int_as_float(0x7fc00000);
-        }
+        a.out_tokens[cell] = -1;
+        a.out_logprobs[cell] = __int_as_float(0x7fc00000);
       }
-      if (tid == 0) report(a.d_status, DS_DEV_ERR_LAYOUT);
+      report(a.d_status, DS_DEV_ERR_LAYOUT);
     }
     return;  // uniform across the cluster; no shared memory was shared yet
   }
@@ -203,24 +289,20 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
     const ReqCursor cur = s_cur;
     const int t = p - cur.off;
     const float g = cur.g, tau = cur.tau;
-    {
-      uint32_t err = 0;
-      if (!(tau >= 0.f) || isnan(g)) err |= DS_DEV_ERR_PARAM;
-      if (g != 0.f && a.u == nullptr) err |= DS_DEV_ERR_NO_UNCOND;
-      if (err) {
-        if (rank == 0 && tid == 0) {
-          a.out_tokens[cell] = -1;
-          a.out_logprobs[cell] = __int_as_float(0x7fc00000);
-          report(a.d_status, err);
-        }
-        __syncthreads();
-        continue;
+    if (!(tau >= 0.f) || isnan(g) || (g != 0.f && a.u == nullptr)) {
+      if (rank == 0 && tid == 0) {
+        a.out_tokens[cell] = -1;
+        a.out_logprobs[cell] = __int_as_float(0x7fc00000);
+        report(a.d_status, (!(tau >= 0.f) || isnan(g)) ? DS_DEV_ERR_PARAM : DS_DEV_ERR_NO_UNCOND);
       }
+      __syncthreads();
+      continue;
     }
     const bool guided = g != 0.f;
     const bool sampled = tau > 0.f;
+    const float2 g2 = make_float2(g, g);
 
-    // ---- slice of the row owned by this CTA
+    // ---- slice of the row owned by this CTA (16-byte chunks of the aligned span)
     const uint16_t* crow = a.c + cell * (long long)V;
     const uintptr_t ca = reinterpret_cast<uintptr_t>(crow);
     const uint4* cb = reinterpret_cast<const uint4*>(ca & ~(uintptr_t)15);
@@ -237,11 +319,12 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
       urow = a.u + ((long long)c * P_u + cur.off_u + t) * (long long)V;
       const uintptr_t ua = reinterpret_cast<uintptr_t>(urow);
       ub = reinterpret_cast<const uint4*>(ua & ~(uintptr_t)15);
-      u_aligned = ((ua & 15) >> 1) == (uintptr_t)dc;
+      u_aligned = (ua & 15) == (ca & 15);
     }
 
-    // ---- pass 1: load, combine, stage z; max and moments
-    float m = -kInf, s1 = 0.f, s2 = 0.f;
+    // ---- pass 1: load, combine, stage z; max and moments (each thread's first chunk)
+    float m = -kInf;
+    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
     int nsub = 0;
     for (int q0 = q_lo + tid; q0 < q_hi; q0 += NT * UNROLL) {
       uint4 vc[UNROLL], vu[UNROLL];
@@ -277,321 +360,244 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
       for (int uu = 0; uu < UNROLL; ++uu) {
         const int q = q0 + uu * NT;
         if (q < q_hi) {
-          float z[8];
-          unpack8(vc[uu], z);
-          if (guided) {
-            float uf[8];
-            unpack8(vu[uu], uf);
+          const uint32_t wc[4] = {vc[uu].x, vc[uu].y, vc[uu].z, vc[uu].w};
+          const uint32_t wu[4] = {vu[uu].x, vu[uu].y, vu[uu].z, vu[uu].w};
+          float2 z[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) z[e] = cfg_combine(z[e], uf[e], g);
+          for (int i = 0; i < 4; ++i) {
+            const float2 cp = make_float2(bf_lo(wc[i]), bf_hi(wc[i]));
+            if (guided) {
+              const float2 up = make_float2(bf_lo(wu[i]), bf_hi(wu[i]));
+              z[i] = __ffma2_rn(g2, __ffma2_rn(up, neg1, cp), cp);  // fl(c - u), then one fma
+            } else {
+              z[i] = cp;
+            }
           }
           if (q == 0 || q >= nq - 1) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int id = 8 * q - dc + e;
-              if (id < 0 || id >= V) z[e] = -kInf;
+            for (int i = 0; i < 4; ++i) {
+              const int id = 8 * q - dc + 2 * i;
+              if (id < 0 || id >= V) z[i].x = -kInf;
+              if (id + 1 < 0 || id + 1 >= V) z[i].y = -kInf;
             }
-          } else if (q0 == q_lo + tid && uu == 0) {
+          } else if (uu == 0 && q0 == q_lo + tid) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              s1 += z[e];
-              s2 = fmaf(z[e], z[e], s2);
+            for (int i = 0; i < 4; ++i) {
+              s1 = __fadd2_rn(s1, z[i]);
+              s2 = __ffma2_rn(z[i], z[i], s2);
             }
             nsub += 8;
           }
 #pragma unroll
-          for (int e = 0; e < 8; ++e) m = fmaxf(m, z[e]);
+          for (int i = 0; i < 4; ++i) m = max3c(m, z[i].x, z[i].y);
           float4* dst = reinterpret_cast<float4*>(zs + 8 * (q - q_lo));
-          dst[0] = make_float4(z[0], z[1], z[2], z[3]);
-          dst[1] = make_float4(z[4], z[5], z[6], z[7]);
+          dst[0] = make_float4(z[0].x, z[0].y, z[1].x, z[1].y);
+          dst[1] = make_float4(z[2].x, z[2].y, z[3].x, z[3].y);
         }
       }
     }
     // R1: max and moments
+    float mu = 0.f, sd = 0.f, tlo = -FLT_MAX, thi = kInf;
     {
-      float f[4] = {m, s1, s2, 0.f};
-      const int fop[4] = {1, 0, 0, 0};
+      float f[4] = {m, s1.x + s1.y, s2.x + s2.y, 0.f};
+      const int fop[4] = {OP_MAX, OP_SUM, OP_SUM, OP_SUM};
       int v[4] = {nsub, 0, 0, 0};
-      const int iop[4] = {0, 0, 0, 0};
-      block_reduce<NT>(red, f, fop, 3, v, iop, 1);
-      Rec r;
-      r.f[0] = f[0]; r.f[1] = f[1]; r.f[2] = f[2]; r.i[0] = v[0];
-      cluster_gather(cl, xs, r, parity, cs);
-    }
-    float S1 = 0.f, S2 = 0.f;
-    int n_s = 0;
-    m = -kInf;
-    for (int j = 0; j < cs; ++j) {
-      m = fmaxf(m, xs.peers[j].f[0]);
-      S1 += xs.peers[j].f[1];
-      S2 += xs.peers[j].f[2];
-      n_s += xs.peers[j].i[0];
-    }
-    if (m == -kInf) {
-      if (rank == 0 && tid == 0) {
-        a.out_tokens[cell] = 0;
-        a.out_logprobs[cell] = __int_as_float(0x7fc00000);
+      const int iop[4] = {OP_SUM, OP_SUM, OP_SUM, OP_SUM};
+      cluster_allreduce<NT>(cl, xs, red, f, fop, 3, v, iop, 1, parity, cs);
+      m = f[0];
+      if (m == -kInf) {
+        if (rank == 0 && tid == 0) {
+          a.out_tokens[cell] = 0;
+          a.out_logprobs[cell] = __int_as_float(0x7fc00000);
+        }
+        __syncthreads();
+        continue;
       }
-      __syncthreads();
-      continue;
-    }
-    float mu = 0.f, sd = 0.f, tlo = -kInf, thi = kInf;
-    bool all_mode = true;
-    if (sampled && n_s >= 64 && a.q_lo > -kInf) {
-      mu = S1 / (float)n_s;
-      sd = sqrtf(fmaxf(S2 / (float)n_s - mu * mu, 0.f));
-      const float guess = fmaf(sd, a.q_lo, mu);
-      if (isfinite(guess)) {
-        tlo = fminf(guess, m);
-        all_mode = false;
-        const float gh = fmaf(sd, a.q_hi, mu);
-        if (isfinite(gh)) thi = gh;
+      if (sampled && v[0] >= 64 && a.q_lo > -kInf) {
+        mu = f[1] / (float)v[0];
+        sd = sqrtf(fmaxf(f[2] / (float)v[0] - mu * mu, 0.f));
+        const float guess = fmaf(sd, a.q_lo, mu);
+        if (isfinite(guess)) {
+          tlo = fminf(guess, m);
+          const float gh = fmaf(sd, a.q_hi, mu);
+          if (isfinite(gh)) thi = gh;
+        }
       }
     }
+    const float2 nml = make_float2(-m * kLog2e, -m * kLog2e);
 
-    // ---- pass 2: logsumexp, threshold counts, argmax
-    float ssum = 0.f;
+    // ---- pass 2: logsumexp, counts above t_lo and t_hi (or the argmax when tau == 0)
+    float2 acc = make_float2(0.f, 0.f);
     int cnt = 0, chi = 0, amin = INT_MAX;
     {
       const float4* z4 = reinterpret_cast<const float4*>(zs);
-      if (sampled) {
-        for (int l4 = tid; l4 < n_loc / 4; l4 += NT) {
-          const float4 v = z4[l4];
-          const float zz[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            ssum += ex2_approx((zz[e] - m) * kLog2e);
-            cnt += (zz[e] >= tlo) ? 1 : 0;
-            chi += (zz[e] >= thi) ? 1 : 0;
-          }
-        }
-      } else {
-        for (int l4 = tid; l4 < n_loc / 4; l4 += NT) {
-          const float4 v = z4[l4];
-          const float zz[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            ssum += ex2_approx((zz[e] - m) * kLog2e);
-            if (zz[e] == m) amin = min(amin, id_base + 4 * l4 + e);
-          }
+      for (int l4 = tid; l4 < n_loc / 4; l4 += NT) {
+        const float4 v = z4[l4];
+        const float2 za = make_float2(v.x, v.y), zb = make_float2(v.z, v.w);
+        const float2 ta = __ffma2_rn(za, l2e, nml), tb = __ffma2_rn(zb, l2e, nml);
+        acc = __fadd2_rn(acc, make_float2(ex2_approx(ta.x), ex2_approx(ta.y)));
+        acc = __fadd2_rn(acc, make_float2(ex2_approx(tb.x), ex2_approx(tb.y)));
+        if (sampled) {
+          cnt += (v.x >= tlo) + (v.y >= tlo) + (v.z >= tlo) + (v.w >= tlo);
+          chi += (v.x >= thi) + (v.y >= thi) + (v.z >= thi) + (v.w >= thi);
+        } else {
+          const int id4 = id_base + 4 * l4;
+          if (v.w == m) amin = id4 + 3;
+          if (v.z == m) amin = id4 + 2;
+          if (v.y == m) amin = id4 + 1;
+          if (v.x == m) amin = id4;
         }
       }
     }
+    float lse;
+    int ctot, chi_tot;
     {
-      float f[4] = {ssum, 0.f, 0.f, 0.f};
-      const int fop[4] = {0, 0, 0, 0};
+      float f[4] = {acc.x + acc.y, 0.f, 0.f, 0.f};
+      const int fop[4] = {OP_SUM, OP_SUM, OP_SUM, OP_SUM};
       int v[4] = {cnt, chi, amin, 0};
-      const int iop[4] = {0, 0, 1, 0};
-      block_reduce<NT>(red, f, fop, 1, v, iop, 3);
-      Rec r;
-      r.f[0] = f[0]; r.i[0] = v[0]; r.i[1] = v[1]; r.i[2] = v[2];
-      cluster_gather(cl, xs, r, parity, cs);
-    }
-    float s_tot = 0.f;
-    int ctot = 0, chi_tot = 0, am = INT_MAX;
-    for (int j = 0; j < cs; ++j) {
-      s_tot += xs.peers[j].f[0];
-      ctot += xs.peers[j].i[0];
-      chi_tot += xs.peers[j].i[1];
-      am = min(am, xs.peers[j].i[2]);
-    }
-    const float lse = m + logf(s_tot);
-    if (!sampled) {
-      if (rank == 0 && tid == 0) {
-        a.out_tokens[cell] = am;
-        a.out_logprobs[cell] = m - lse;
+      const int iop[4] = {OP_SUM, OP_SUM, OP_MIN, OP_SUM};
+      cluster_allreduce<NT>(cl, xs, red, f, fop, 1, v, iop, 3, parity, cs);
+      lse = m + logf(f[0]);
+      ctot = v[0];
+      chi_tot = v[1];
+      if (!sampled) {
+        if (rank == 0 && tid == 0) {
+          a.out_tokens[cell] = v[2];
+          a.out_logprobs[cell] = m - lse;
+        }
+        __syncthreads();
+        continue;
       }
-      __syncthreads();
-      continue;
     }
 
-    // ---- threshold verification (rare recount), then compaction
-    if (!all_mode && ctot < k) {
-      const float guess = fmaf(sd, a.q_lo - 1.0f, mu);
-      all_mode = true;
-      if (isfinite(guess) && guess < tlo) {
-        tlo = guess;
-        cnt = 0;
-        const float4* z4 = reinterpret_cast<const float4*>(zs);
-        for (int l4 = tid; l4 < n_loc / 4; l4 += NT) {
-          const float4 v = z4[l4];
-          cnt += (v.x >= tlo) + (v.y >= tlo) + (v.z >= tlo) + (v.w >= tlo);
-        }
-        float f[4] = {0.f, 0.f, 0.f, 0.f};
-        const int fop[4] = {0, 0, 0, 0};
-        int v[4] = {cnt, 0, 0, 0};
-        const int iop[4] = {0, 0, 0, 0};
-        block_reduce<NT>(red, f, fop, 0, v, iop, 1);
-        Rec r;
-        r.i[0] = v[0];
-        cluster_gather(cl, xs, r, parity, cs);
-        ctot = 0;
-        for (int j = 0; j < cs; ++j) ctot += xs.peers[j].i[0];
-        all_mode = ctot < k;
-      }
-    }
-    if (all_mode) {
+    // ---- the guess must cover the top k; otherwise keep every finite element
+    if (ctot < k && tlo > -FLT_MAX) {
+      tlo = -FLT_MAX;
       cnt = 0;
-      for (int l4 = tid; l4 < n_loc / 4; l4 += NT)
-        for (int e = 0; e < 4; ++e) {
-          const int id = id_base + 4 * l4 + e;
-          cnt += (id >= 0 && id < V) ? 1 : 0;
-        }
-      ctot = V;
+      const float4* z4 = reinterpret_cast<const float4*>(zs);
+      for (int l4 = tid; l4 < n_loc / 4; l4 += NT) {
+        const float4 v = z4[l4];
+        cnt += (v.x >= tlo) + (v.y >= tlo) + (v.z >= tlo) + (v.w >= tlo);
+      }
+      ctot = cluster_sum<NT>(cl, xs, red, cnt, parity, cs);
     }
+    // compaction of this CTA's candidates (local indices)
     int nL = 0;
     {
       int pos = block_excl_scan<NT>(wsum, cnt, nL);
       const float4* z4 = reinterpret_cast<const float4*>(zs);
       for (int l4 = tid; l4 < n_loc / 4; l4 += NT) {
         const float4 v = z4[l4];
-        const float zz[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int l = 4 * l4 + e;
-          const int id = id_base + l;
-          const bool keep = all_mode ? (id >= 0 && id < V) : (zz[e] >= tlo);
-          if (keep) idxs[pos++] = (uint16_t)l;
-        }
+        const int l = 4 * l4;
+        // predicated stores: the slot after this thread's last candidate belongs to the next thread
+        if (v.x >= tlo) idxs[pos++] = (uint16_t)l;
+        if (v.y >= tlo) idxs[pos++] = (uint16_t)(l + 1);
+        if (v.z >= tlo) idxs[pos++] = (uint16_t)(l + 2);
+        if (v.w >= tlo) idxs[pos++] = (uint16_t)(l + 3);
       }
     }
     __syncthreads();
 
-    // ---- Gumbel race (R3): table bounds, cluster-wide candidates
+    // ---- Gumbel race: table bounds per candidate, cluster-wide top-2 by upper bound
     const uint32_t t32 = (uint32_t)t;
     const uint32_t ctr3 = a.iter_hi | (uint32_t)c;
-    float loMax = -kInf;
-    Top2 tp;
-    top2_init(tp);
-    for (int i = tid; i < nL; i += NT) {
-      const int l = idxs[i];
-      const float zi = zs[l];
-      const int id = id_base + l;
-      const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
-      const float2 gb = gumbel_bounds(x);
-      const float lo = __fmaf_rn(tau, gb.x, zi);
-      const float hi = __fmaf_rn(tau, gb.y, zi);
-      loMax = fmaxf(loMax, lo);
-      top2_insert(tp, hi, zi, id, x);
-    }
-    loMax = warp_max(loMax);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const Top2 u = top2_shfl(tp, o);
-      top2_merge(tp, u);
-    }
-    __syncthreads();
-    if (lane == 0) {
-      wtop[wid] = tp;
-      red.f[wid][0] = loMax;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      Top2 b = wtop[0];
-      float lm = red.f[0][0];
-      for (int w = 1; w < NT / 32; ++w) {
-        top2_merge(b, wtop[w]);
-        lm = fmaxf(lm, red.f[w][0]);
-      }
-      Rec r;
-      r.f[0] = lm;
-      r.f[1] = b.hA; r.f[2] = b.zA; r.i[0] = b.idA; r.i[1] = (int)b.xA;
-      r.f[3] = b.hB; r.f[4] = b.zB; r.i[2] = b.idB; r.i[3] = (int)b.xB;
-      r.f[5] = b.h3;
-      xs.slot[parity] = r;
-    }
+    const float2 tau2 = make_float2(tau, tau);
     {
-      // gather (the record was written by thread 0 above)
+      float loMax = -kInf;
+      Top2 tp;
+      top2_init(tp);
+      for (int i = tid; i < nL; i += NT) {
+        const int l = idxs[i];
+        const float zi = zs[l];
+        const int id = id_base + l;
+        const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
+        const float2 sc2 = __ffma2_rn(tau2, gumbel_bounds(x), make_float2(zi, zi));
+        loMax = fmaxf(loMax, sc2.x);
+        top2_insert(tp, sc2.y, zi, id, x);
+      }
+      loMax = warp_max(loMax);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) top2_merge(tp, top2_shfl(tp, o));
+      __syncthreads();
+      if (lane == 0) {
+        wtop[wid] = tp;
+        red.f[wid][0] = loMax;
+      }
+      __syncthreads();
+      if (wid == 0) {
+        Top2 b;
+        top2_init(b);
+        float lm = -kInf;
+        if (lane < NT / 32) {
+          b = wtop[lane];
+          lm = red.f[lane][0];
+        }
+        lm = warp_max(lm);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) top2_merge(b, top2_shfl(b, o));
+        if (lane == 0) {
+          Rec r;
+          r.f[0] = lm;
+          r.f[1] = b.hA; r.f[2] = b.zA; r.i[0] = b.idA; r.i[1] = (int)b.xA;
+          r.f[3] = b.hB; r.f[4] = b.zB; r.i[2] = b.idB; r.i[3] = (int)b.xB;
+          r.f[5] = b.h3;
+          xs.slot[parity] = r;
+        }
+      }
       cl.sync();
-      if (tid < cs) xs.peers[tid] = *cl.map_shared_rank(&xs.slot[parity], tid);
+      if (wid == 0) {
+        Top2 b;
+        top2_init(b);
+        float lm = -kInf;
+        if (lane < cs) {
+          const Rec* src = cl.map_shared_rank(&xs.slot[parity], lane);
+          lm = src->f[0];
+          b.hA = src->f[1]; b.zA = src->f[2]; b.idA = src->i[0]; b.xA = (uint32_t)src->i[1];
+          b.hB = src->f[3]; b.zB = src->f[4]; b.idB = src->i[2]; b.xB = (uint32_t)src->i[3];
+          b.h3 = src->f[5];
+        }
+        lm = warp_max(lm);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) top2_merge(b, top2_shfl(b, o));
+        if (lane == 0) {
+          xs.ctop = b;
+          xs.cS = lm;
+        }
+      }
       __syncthreads();
       parity ^= 1;
     }
-    float S = -kInf;
-    for (int j = 0; j < cs; ++j) S = fmaxf(S, xs.peers[j].f[0]);
+    const float S = xs.cS;
+    const Top2 ct = xs.ctop;
     bool exact = !(S > -kInf);
     float zw = 0.f;
     int idw = -1;
     if (!exact) {
       const float thr = S - (fabsf(S) + 1.f) * 0x1p-20f;
-      int n_cand = 0;
-      bool any_cplx = false;
-      for (int j = 0; j < cs; ++j) {
-        const Rec& r = xs.peers[j];
-        if (r.i[0] >= 0 && r.f[1] >= thr) {
-          ++n_cand;
-          zw = r.f[2];
-          idw = r.i[0];
-        }
-        if (r.i[2] >= 0 && r.f[3] >= thr) {
-          ++n_cand;
-          zw = r.f[4];
-          idw = r.i[2];
-        }
-        if (r.f[5] >= thr) any_cplx = true;
-      }
-      if (!(n_cand == 1 && !any_cplx)) {
-        // R4: exact Gumbel values for the candidates the bounds cannot separate
-        const Rec& me = xs.peers[rank];
-        const bool my_cplx = me.f[5] >= thr;
+      const bool ca_ = ct.idA >= 0 && ct.hA >= thr;
+      const bool cb_ = ct.idB >= 0 && ct.hB >= thr;
+      if (ca_ && !cb_ && !(ct.h3 >= thr)) {
+        zw = ct.zA;
+        idw = ct.idA;
+      } else {
+        // exact G for every candidate the bounds cannot separate
         float bs = -kInf, bz = 0.f;
         int bid = INT_MAX;
-        if (my_cplx) {
-          for (int i = tid; i < nL; i += NT) {
-            const int l = idxs[i];
-            const float zi = zs[l];
-            const int id = id_base + l;
-            const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
-            const float hi = __fmaf_rn(tau, gumbel_bounds(x).y, zi);
-            if (hi >= thr) {
-              const float sc = __fmaf_rn(tau, gumbel_accurate(x), zi);
-              if (sc > bs || (sc == bs && id < bid) || bid == INT_MAX) {
-                bs = sc; bz = zi; bid = id;
-              }
+        for (int i = tid; i < nL; i += NT) {
+          const int l = idxs[i];
+          const float zi = zs[l];
+          const int id = id_base + l;
+          const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
+          if (__fmaf_rn(tau, gumbel_bounds(x).y, zi) >= thr) {
+            const float scr = __fmaf_rn(tau, gumbel_accurate(x), zi);
+            if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
+              bs = scr; bz = zi; bid = id;
             }
           }
-        } else if (tid < 2) {
-          const int idc = tid == 0 ? me.i[0] : me.i[2];
-          const float hc = tid == 0 ? me.f[1] : me.f[3];
-          const float zc = tid == 0 ? me.f[2] : me.f[4];
-          const uint32_t xc = (uint32_t)(tid == 0 ? me.i[1] : me.i[3]);
-          if (idc >= 0 && hc >= thr) {
-            bs = __fmaf_rn(tau, gumbel_accurate(xc), zc);
-            bz = zc;
-            bid = idc;
-          }
         }
-        // block argmax (score desc, id asc)
-        const int wl = warp_argmax_lane(bs, bid);
-        const float wbs = __shfl_sync(0xffffffffu, bs, wl);
-        const float wbz = __shfl_sync(0xffffffffu, bz, wl);
-        const int wbid = __shfl_sync(0xffffffffu, bid, wl);
-        __syncthreads();
-        if (lane == 0) {
-          red.f[wid][0] = wbs; red.f[wid][1] = wbz; red.i[wid][0] = wbid;
-        }
-        __syncthreads();
-        Rec r;
-        r.f[0] = red.f[0][0]; r.f[1] = red.f[0][1]; r.i[0] = red.i[0][0];
-        for (int w = 1; w < NT / 32; ++w) {
-          const float os = red.f[w][0];
-          const int oi = red.i[w][0];
-          if (os > r.f[0] || (os == r.f[0] && oi < r.i[0])) {
-            r.f[0] = os; r.f[1] = red.f[w][1]; r.i[0] = oi;
-          }
-        }
-        cluster_gather(cl, xs, r, parity, cs);
-        float best = xs.peers[0].f[0];
-        zw = xs.peers[0].f[1];
-        idw = xs.peers[0].i[0];
-        for (int j = 1; j < cs; ++j) {
-          const Rec& q = xs.peers[j];
-          if (q.f[0] > best || (q.f[0] == best && q.i[0] < idw)) {
-            best = q.f[0]; zw = q.f[1]; idw = q.i[0];
-          }
-        }
+        cluster_argmax<NT>(cl, xs, red, bs, bid, bz, zw, idw, parity, cs);
       }
-      // R5: the winner must rank inside the exact top-k (rank by (z desc, id asc))
+      // the winner must rank inside the exact top-k (rank by (z desc, id asc))
       if (ctot > k && !(chi_tot <= k && zw >= thi)) {
         int rr = 0;
         for (int i = tid; i < nL; i += NT) {
@@ -599,40 +605,22 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
           const float zi = zs[l];
           rr += (zi > zw || (zi == zw && id_base + l < idw)) ? 1 : 0;
         }
-        float f[4] = {0.f, 0.f, 0.f, 0.f};
-        const int fop[4] = {0, 0, 0, 0};
-        int v[4] = {rr, 0, 0, 0};
-        const int iop[4] = {0, 0, 0, 0};
-        block_reduce<NT>(red, f, fop, 0, v, iop, 1);
-        Rec r;
-        r.i[0] = v[0];
-        cluster_gather(cl, xs, r, parity, cs);
-        int rank_w = 0;
-        for (int j = 0; j < cs; ++j) rank_w += xs.peers[j].i[0];
-        if (rank_w >= k) exact = true;
+        if (cluster_sum<NT>(cl, xs, red, rr, parity, cs) >= k) exact = true;
       }
     }
     if (exact) {
-      // Exact kept set: the k-th largest composite key, one bit per cluster round.
+      // exact kept set: the k-th largest composite key, one bit per cluster round
       unsigned long long kth = 0ull;
-      for (int b = 63; b >= 0; --b) {
-        const unsigned long long probe = kth | (1ull << b);
-        int cb2 = 0;
-        for (int i = tid; i < nL; i += NT) {
-          const int l = idxs[i];
-          cb2 += (rank_key(zs[l], id_base + l) >= probe) ? 1 : 0;
+      if (ctot > k) {
+        for (int b = 63; b >= 0; --b) {
+          const unsigned long long probe = kth | (1ull << b);
+          int cb2 = 0;
+          for (int i = tid; i < nL; i += NT) {
+            const int l = idxs[i];
+            cb2 += (rank_key(zs[l], id_base + l) >= probe) ? 1 : 0;
+          }
+          if (cluster_sum<NT>(cl, xs, red, cb2, parity, cs) >= k) kth = probe;
         }
-        float f[4] = {0.f, 0.f, 0.f, 0.f};
-        const int fop[4] = {0, 0, 0, 0};
-        int v[4] = {cb2, 0, 0, 0};
-        const int iop[4] = {0, 0, 0, 0};
-        block_reduce<NT>(red, f, fop, 0, v, iop, 1);
-        Rec r;
-        r.i[0] = v[0];
-        cluster_gather(cl, xs, r, parity, cs);
-        int tot = 0;
-        for (int j = 0; j < cs; ++j) tot += xs.peers[j].i[0];
-        if (tot >= k) kth = probe;
       }
       float bs = -kInf, bz = 0.f;
       int bid = INT_MAX;
@@ -642,40 +630,13 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
         const int id = id_base + l;
         if (rank_key(zi, id) >= kth) {
           const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
-          const float sc = __fmaf_rn(tau, gumbel_accurate(x), zi);
-          if (bid == INT_MAX || sc > bs || (sc == bs && id < bid)) {
-            bs = sc; bz = zi; bid = id;
+          const float scr = __fmaf_rn(tau, gumbel_accurate(x), zi);
+          if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
+            bs = scr; bz = zi; bid = id;
           }
         }
       }
-      const int wl = warp_argmax_lane(bs, bid);
-      const float wbs = __shfl_sync(0xffffffffu, bs, wl);
-      const float wbz = __shfl_sync(0xffffffffu, bz, wl);
-      const int wbid = __shfl_sync(0xffffffffu, bid, wl);
-      __syncthreads();
-      if (lane == 0) {
-        red.f[wid][0] = wbs; red.f[wid][1] = wbz; red.i[wid][0] = wbid;
-      }
-      __syncthreads();
-      Rec r;
-      r.f[0] = red.f[0][0]; r.f[1] = red.f[0][1]; r.i[0] = red.i[0][0];
-      for (int w = 1; w < NT / 32; ++w) {
-        const float os = red.f[w][0];
-        const int oi = red.i[w][0];
-        if (os > r.f[0] || (os == r.f[0] && oi < r.i[0])) {
-          r.f[0] = os; r.f[1] = red.f[w][1]; r.i[0] = oi;
-        }
-      }
-      cluster_gather(cl, xs, r, parity, cs);
-      float best = xs.peers[0].f[0];
-      zw = xs.peers[0].f[1];
-      idw = xs.peers[0].i[0];
-      for (int j = 1; j < cs; ++j) {
-        const Rec& q = xs.peers[j];
-        if (q.f[0] > best || (q.f[0] == best && q.i[0] < idw)) {
-          best = q.f[0]; zw = q.f[1]; idw = q.i[0];
-        }
-      }
+      cluster_argmax<NT>(cl, xs, red, bs, bid, bz, zw, idw, parity, cs);
     }
     if (rank == 0 && tid == 0) {
       a.out_tokens[cell] = idw;
@@ -689,7 +650,7 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
 // ---------------------------------------------------------------- launcher
 namespace {
 constexpr int kClusterNT = 256;
-constexpr int kClusterUnroll = 4;
+constexpr int kClusterUnroll = 8;
 constexpr int kSliceCapMax = 16384;
 }  // namespace
 

@@ -1,24 +1,28 @@
 // k_sample_warp.cu -- sampling pass for small vocabularies: one warp per cell.
 //
-// A cell's whole row (V <= 8 * 256 - 7 elements) is loaded with 16-byte
-// streaming loads and kept in registers as fp32 z; every later step (max,
-// logsumexp, the top-ratio cut and the Gumbel race) runs on-chip, so the
-// logits are read from HBM exactly once. Warps own contiguous cell ranges, so
-// the position -> request walk advances in O(1) per cell.
+// A cell's row (V <= 2055) is read once from HBM with 16-byte streaming loads
+// and kept in registers as fp32 z: each lane owns NCH aligned 16-byte chunks
+// (8 elements each) plus at most one scalar element from the unaligned head or
+// tail of the row. Every later step (max, logsumexp, the top-ratio cut, the
+// Gumbel race) runs on-chip. Warps own contiguous cell ranges, so the position
+// -> request walk advances in O(1) per cell.
 //
 // Steps per cell ("Sampler support for discrete diffusion", Hert4's first
 // comment; "Add a sampler resource for discrete diffusion", Contract):
-//   1. z = c + g (c - u)                 (u skipped for g == 0)
-//   2. m = max z, lse = m + log sum exp(z - m), argmax (tau == 0)
-//   3. kept set = k largest z, ties to the smallest id: a lower threshold
-//      t_lo is guessed from the row's moments, verified by counting
-//      (count(z >= t_lo) >= k) and the candidates compacted to shared memory
+//   1. z = c + g (c - u)                 (u skipped for g == 0), row max,
+//                                        moments of a subsample
+//   2. lse = m + log sum exp(z - m) and, in the same sweep, every element with
+//      z >= t_lo is written to a per-lane column of shared memory (the store
+//      is unconditional, the column pointer advances only for kept elements),
+//      t_lo being a threshold guessed from the moments
+//   3. the guess is verified exactly: count(z >= t_lo) >= k, so the kept set
+//      (the k largest z, ties to the smallest id) lies inside the candidates
 //   4. Gumbel race over the candidates: table bounds on G settle the winner
-//      unless the bounds overlap, in which case G is evaluated exactly for the
-//      overlapping few; the winner's membership in the exact top-k is
-//      checked by its rank, and a rare miss falls back to an exact 64-bit
-//      radix select of the k-th key
+//      unless they overlap, in which case G is evaluated exactly for the few
+//      that overlap; the winner's membership in the exact top-k is checked by
+//      its rank, and a rare miss falls back to an exact 64-bit radix select
 //   5. (token, logprob = z_tok - lse)
+#include <cfloat>
 #include <climits>
 
 #include "ds_launch.h"
@@ -26,16 +30,51 @@
 
 namespace ds {
 
+constexpr int kDenseCap = 256;  // candidates gathered into one balanced list
+
 template <int NCH>
-__global__ void __launch_bounds__(kWarpKernelThreads) k_sample_warp(const SampleArgs a) {
+struct WarpSmem {
+  float2 col[NCH * 8 + 1][32];  // per-lane candidate columns: (z, id as int bits)
+  float2 dense[kDenseCap];      // balanced candidate list
+};
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Iterates over this lane's share of the candidates: a balanced slice of the
+// dense list, or (when it overflowed) the lane's own column.
+struct Items {
+  bool dense;
+  int n;      // dense: candidate count; column: this lane's count
+  int n_it;   // iterations the warp runs
+  __device__ __forceinline__ bool get(const float2 (*col)[32], const float2* dl, int it, int lane,
+                                      float2& v) const {
+    if (dense) {
+      const int i = lane + 32 * it;
+      if (i >= n) return false;
+      v = dl[i];
+      return true;
+    }
+    if (it >= n) return false;
+    v = col[it][lane];
+    return true;
+  }
+};
+
+// Register budget per thread: 4 CTAs of 4 warps per SM up to NCH = 4.
+template <int NCH>
+__global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 6) ? 3 : 2))
+    k_sample_warp(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  WarpSmem<NCH>& sm = reinterpret_cast<WarpSmem<NCH>*>(smem_raw)[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
-  const int wib = threadIdx.x >> 5;
-  float2* Lb = reinterpret_cast<float2*>(smem_raw) + (size_t)wib * (NCH * 256);
 
   const long long n_cells = (long long)a.C * a.P;
   const long long nw = (long long)gridDim.x * (kWarpKernelThreads / 32);
-  const long long gw = (long long)blockIdx.x * (kWarpKernelThreads / 32) + wib;
+  const long long gw = (long long)blockIdx.x * (kWarpKernelThreads / 32) + (threadIdx.x >> 5);
   const long long cbeg = gw * n_cells / nw;
   const long long cend = (gw + 1) * n_cells / nw;
   if (cbeg >= cend) return;
@@ -51,17 +90,20 @@ __global__ void __launch_bounds__(kWarpKernelThreads) k_sample_warp(const Sample
     return;
   }
   const long long P_u = bt.tot_u;
+  const float2 neg1 = make_float2(-1.f, -1.f);
+  const float2 l2e = make_float2(kLog2e, kLog2e);
 
   ReqCursor cur;
-  cur.r = -1;
-  int cur_c = -1;
+  int c = (int)(cbeg / P);
+  int p = (int)(cbeg - (long long)c * P);
+  warp_find_request(a, p, lane, cur);
 
   for (long long cell = cbeg; cell < cend; ++cell) {
-    const int c = (int)(cell / P);
-    const int p = (int)(cell - (long long)c * P);
-    if (c != cur_c || cur.r < 0 || p < cur.off) {
-      warp_find_request(a, p, lane, cur);  // always found: the totals were checked
-      cur_c = c;
+    // ---- position -> request (advance; restart at the next row)
+    if (p == P) {
+      p = 0;
+      ++c;
+      warp_find_request(a, 0, lane, cur);
     }
     while (p >= cur.off + cur.T) {
       cur.off += cur.T;
@@ -73,97 +115,101 @@ __global__ void __launch_bounds__(kWarpKernelThreads) k_sample_warp(const Sample
       cur.rid = (uint32_t)a.request_ids[cur.r];
     }
     const int t = p - cur.off;
+    ++p;
     const float g = cur.g, tau = cur.tau;
-    {
-      uint32_t err = 0;
-      if (!(tau >= 0.f) || isnan(g)) err |= DS_DEV_ERR_PARAM;
-      if (g != 0.f && a.u == nullptr) err |= DS_DEV_ERR_NO_UNCOND;
-      if (err) {
-        if (lane == 0) {
-          a.out_tokens[cell] = -1;
-          a.out_logprobs[cell] = __int_as_float(0x7fc00000);
-          report(a.d_status, err);
-        }
-        continue;
+    if (!(tau >= 0.f) || isnan(g) || (g != 0.f && a.u == nullptr)) {
+      if (lane == 0) {
+        a.out_tokens[cell] = -1;
+        a.out_logprobs[cell] = __int_as_float(0x7fc00000);
+        report(a.d_status, (!(tau >= 0.f) || isnan(g)) ? DS_DEV_ERR_PARAM : DS_DEV_ERR_NO_UNCOND);
       }
+      continue;
     }
 
-    // ---- load the row (16-byte chunks of the aligned span covering it)
+    // ---- row geometry: h head elements, nfc aligned full chunks, ns scalar elements
     const uint16_t* crow = a.c + cell * (long long)V;
     const uintptr_t ca = reinterpret_cast<uintptr_t>(crow);
-    const uint4* cb = reinterpret_cast<const uint4*>(ca & ~(uintptr_t)15);
-    const int dc = (int)((ca & 15) >> 1);  // elements of the first chunk before the row
-    const int nq = (dc + V + 7) >> 3;      // chunks covering the row
+    const int h = min((int)(((16u - (unsigned)(ca & 15)) & 15u) >> 1), V);
+    const int nfc = (V - h) >> 3;
+    const int ns = V - 8 * nfc;
+    const uint4* cb = reinterpret_cast<const uint4*>(ca + 2 * (uintptr_t)h);
+    const int sid = (lane < h) ? lane : lane + 8 * nfc;  // this lane's scalar element id (if lane < ns)
+    const bool guided = g != 0.f;
+
     uint4 rc[NCH], ru[NCH];
+    uint32_t sc = 0, su = 0;
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
       const int q = lane + 32 * j;
-      rc[j] = (q < nq) ? ld_stream16(cb + q) : make_uint4(0u, 0u, 0u, 0u);
+      rc[j] = (q < nfc) ? ld_stream16(cb + q) : make_uint4(0u, 0u, 0u, 0u);
     }
-    const bool guided = g != 0.f;
+    if (lane < ns) sc = __ldg(crow + sid);
     if (guided) {
       const uint16_t* urow = a.u + ((long long)c * P_u + cur.off_u + t) * (long long)V;
       const uintptr_t ua = reinterpret_cast<uintptr_t>(urow);
-      if (((ua & 15) >> 1) == (uintptr_t)dc) {
-        const uint4* ub = reinterpret_cast<const uint4*>(ua & ~(uintptr_t)15);
+      if ((ua & 15) == (ca & 15)) {
+        const uint4* ub = reinterpret_cast<const uint4*>(ua + 2 * (uintptr_t)h);
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
           const int q = lane + 32 * j;
-          ru[j] = (q < nq) ? ld_stream16(ub + q) : make_uint4(0u, 0u, 0u, 0u);
+          ru[j] = (q < nfc) ? ld_stream16(ub + q) : make_uint4(0u, 0u, 0u, 0u);
         }
       } else {
         // u row aligned differently from the c row: gather element by element.
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
-          const int id0 = 8 * (lane + 32 * j) - dc;
-          uint32_t w[4];
+          const int q = lane + 32 * j;
+          uint32_t w[4] = {0u, 0u, 0u, 0u};
+          if (q < nfc) {
+            const uint16_t* src = urow + h + 8 * q;
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int i0 = id0 + 2 * h, i1 = i0 + 1;
-            const uint32_t lo = (i0 >= 0 && i0 < V) ? (uint32_t)__ldg(urow + i0) : 0u;
-            const uint32_t hi = (i1 >= 0 && i1 < V) ? (uint32_t)__ldg(urow + i1) : 0u;
-            w[h] = lo | (hi << 16);
+            for (int hh = 0; hh < 4; ++hh)
+              w[hh] = (uint32_t)__ldg(src + 2 * hh) | ((uint32_t)__ldg(src + 2 * hh + 1) << 16);
           }
           ru[j] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
+      if (lane < ns) su = __ldg(urow + sid);
     }
 
-    // ---- step 1/2a: z, row max, moments of the interior chunks
-    float z[NCH][8];
-    float m = -kInf, s1 = 0.f, s2 = 0.f;
-    int nsub = 0;
+    // ---- step 1: z, row max, moments of chunks 0..NCH-2 (always full)
+    float2 z[NCH][4];
+    float zs1;
+    const float2 g2 = make_float2(g, g);
+    float m = -kInf;
+    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
-      const int q = lane + 32 * j;
-      float cf[8];
-      unpack8(rc[j], cf);
-      if (guided) {
-        float uf[8];
-        unpack8(ru[j], uf);
+      const uint32_t wc[4] = {rc[j].x, rc[j].y, rc[j].z, rc[j].w};
+      const uint32_t wu[4] = {ru[j].x, ru[j].y, ru[j].z, ru[j].w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) z[j][e] = cfg_combine(cf[e], uf[e], g);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) z[j][e] = cf[e];
-      }
-      if (q == 0 || q >= nq - 1) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int id = 8 * q - dc + e;
-          if (id < 0 || id >= V) z[j][e] = -kInf;
+      for (int i = 0; i < 4; ++i) {
+        const float2 cp = make_float2(bf_lo(wc[i]), bf_hi(wc[i]));
+        if (guided) {
+          const float2 up = make_float2(bf_lo(wu[i]), bf_hi(wu[i]));
+          z[j][i] = __ffma2_rn(g2, __ffma2_rn(up, neg1, cp), cp);  // fl(c - u), then one fma
+        } else {
+          z[j][i] = cp;
         }
       }
+      if (j == NCH - 1 && !(lane + 32 * j < nfc)) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) m = fmaxf(m, z[j][e]);
-      if (j >= 1 && j <= NCH - 2 && q < nq - 1) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          s1 += z[j][e];
-          s2 = fmaf(z[j][e], z[j][e], s2);
-        }
-        nsub += 8;
+        for (int i = 0; i < 4; ++i) z[j][i] = make_float2(-kInf, -kInf);
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m = max3(m, z[j][i].x, z[j][i].y);
+      if (j < NCH - 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          s1 = __fadd2_rn(s1, z[j][i]);
+          s2 = __ffma2_rn(z[j][i], z[j][i], s2);
+        }
+      }
+    }
+    {
+      const float cf = __uint_as_float(sc << 16);
+      zs1 = (lane < ns) ? (guided ? cfg_combine(cf, __uint_as_float(su << 16), g) : cf) : -kInf;
+      m = fmaxf(m, zs1);
     }
     m = warp_max(m);
     if (m == -kInf) {  // every logit is -inf: token 0, logprob NaN
@@ -173,46 +219,30 @@ __global__ void __launch_bounds__(kWarpKernelThreads) k_sample_warp(const Sample
       }
       continue;
     }
+    const float2 nml = make_float2(-m * kLog2e, -m * kLog2e);
+    const int idb = h + 8 * lane;  // id of element (j, 0) is idb + 256 j
 
-    const bool sampled = tau > 0.f;
-    float mu = 0.f, sd = 0.f, tlo = -kInf;
-    bool all_mode = true;
-    if (sampled) {
-      const int n_s = warp_sum_i(nsub);
-      const float S1 = warp_sum(s1), S2 = warp_sum(s2);
-      if (n_s >= 64 && a.q_lo > -kInf) {
-        mu = S1 / (float)n_s;
-        sd = sqrtf(fmaxf(S2 / (float)n_s - mu * mu, 0.f));
-        const float guess = fmaf(sd, a.q_lo, mu);
-        if (isfinite(guess)) {
-          tlo = fminf(guess, m);
-          all_mode = false;
-        }
-      }
-    }
-
-    // ---- step 2b: logsumexp, count above t_lo (or argmax for tau == 0)
-    float ssum = 0.f;
-    int cnt = 0;
-    int amin = INT_MAX;
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        ssum += ex2_approx((z[j][e] - m) * kLog2e);
-        cnt += (z[j][e] >= tlo) ? 1 : 0;
-      }
-    }
-    const float lse = m + logf(warp_sum(ssum));
-    if (!sampled) {
+    // ---- tau == 0: logsumexp and the smallest id attaining the max
+    if (!(tau > 0.f)) {
+      float2 acc = make_float2(0.f, 0.f);
+      int am = INT_MAX;
 #pragma unroll
       for (int j = NCH - 1; j >= 0; --j) {
 #pragma unroll
-        for (int e = 7; e >= 0; --e) {
-          if (z[j][e] == m) amin = 8 * (lane + 32 * j) - dc + e;
+        for (int i = 3; i >= 0; --i) {
+          const float2 tt = __ffma2_rn(z[j][i], l2e, nml);
+          acc = __fadd2_rn(acc, make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
+          if (z[j][i].y == m) am = idb + 256 * j + 2 * i + 1;
+          if (z[j][i].x == m) am = idb + 256 * j + 2 * i;
         }
       }
-      const int am = warp_min_i(amin);
+      float ssum = acc.x + acc.y;
+      if (lane < ns) {
+        ssum += ex2_approx((zs1 - m) * kLog2e);
+        if (zs1 == m) am = min(am, sid);
+      }
+      const float lse = m + logf(warp_sum(ssum));
+      am = warp_min_i(am);
       if (lane == 0) {
         a.out_tokens[cell] = am;
         a.out_logprobs[cell] = m - lse;
@@ -220,160 +250,192 @@ __global__ void __launch_bounds__(kWarpKernelThreads) k_sample_warp(const Sample
       continue;
     }
 
-    // ---- step 3: verify the threshold guess and compact the candidates
-    int ctot;
-    if (!all_mode) {
+    // ---- threshold guess from the subsample moments
+    float mu = 0.f, sd = 0.f, tlo = -FLT_MAX;  // -FLT_MAX: keep every finite element
+    bool guessed = false;
+    if (NCH >= 2 && a.q_lo > -kInf) {
+      const float n_s = (float)(32 * 8 * (NCH > 1 ? NCH - 1 : 1));
+      const float S1 = warp_sum(s1.x + s1.y), S2 = warp_sum(s2.x + s2.y);
+      mu = S1 / n_s;
+      sd = sqrtf(fmaxf(S2 / n_s - mu * mu, 0.f));
+      const float guess = fmaf(sd, a.q_lo, mu);
+      if (isfinite(guess)) {
+        tlo = fminf(guess, m);
+        guessed = true;
+      }
+    }
+
+    // ---- step 2: logsumexp and speculative compaction of z >= t_lo into this lane's column
+    float2* colp = &sm.col[0][lane];
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 zz = z[j][i];
+        const float2 tt = __ffma2_rn(zz, l2e, nml);
+        acc = __fadd2_rn(acc, make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
+        const int id0 = idb + 256 * j + 2 * i;
+        *colp = make_float2(zz.x, __int_as_float(id0));
+        colp += (zz.x >= tlo) ? 32 : 0;
+        *colp = make_float2(zz.y, __int_as_float(id0 + 1));
+        colp += (zz.y >= tlo) ? 32 : 0;
+      }
+    }
+    float ssum = acc.x + acc.y;
+    if (lane < ns) {
+      ssum += ex2_approx((zs1 - m) * kLog2e);
+      *colp = make_float2(zs1, __int_as_float(sid));
+      colp += (zs1 >= tlo) ? 32 : 0;
+    }
+    const float lse = m + logf(warp_sum(ssum));
+    int cnt = (int)(colp - &sm.col[0][lane]) >> 5;
+    int ctot = warp_sum_i(cnt);
+
+    // ---- step 3: the guess must cover the top k; otherwise keep every finite element
+    if (guessed && ctot < k) {
+      tlo = -FLT_MAX;
+      colp = &sm.col[0][lane];
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int id0 = idb + 256 * j + 2 * i;
+          *colp = make_float2(z[j][i].x, __int_as_float(id0));
+          colp += (z[j][i].x >= tlo) ? 32 : 0;
+          *colp = make_float2(z[j][i].y, __int_as_float(id0 + 1));
+          colp += (z[j][i].y >= tlo) ? 32 : 0;
+        }
+      }
+      if (lane < ns) {
+        *colp = make_float2(zs1, __int_as_float(sid));
+        colp += (zs1 >= tlo) ? 32 : 0;
+      }
+      cnt = (int)(colp - &sm.col[0][lane]) >> 5;
       ctot = warp_sum_i(cnt);
-      if (ctot < k) {
-        const float guess = fmaf(sd, a.q_lo - 1.0f, mu);
-        all_mode = true;
-        if (isfinite(guess) && guess < tlo) {
-          tlo = guess;
-          cnt = 0;
-#pragma unroll
-          for (int j = 0; j < NCH; ++j)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) cnt += (z[j][e] >= tlo) ? 1 : 0;
-          ctot = warp_sum_i(cnt);
-          all_mode = ctot < k;
-        }
-      }
-    }
-    if (all_mode) {
-      cnt = 0;
-#pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        const int id0 = 8 * (lane + 32 * j) - dc;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) cnt += (id0 + e >= 0 && id0 + e < V) ? 1 : 0;
-      }
-      ctot = V;
-    }
-    {
-      int pos = warp_excl_scan(cnt, lane);
-#pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        const int id0 = 8 * (lane + 32 * j) - dc;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int id = id0 + e;
-          const bool keep = all_mode ? (id >= 0 && id < V) : (z[j][e] >= tlo);
-          if (keep) {
-            Lb[pos] = make_float2(z[j][e], __int_as_float(id));
-            ++pos;
-          }
-        }
-      }
     }
     __syncwarp();
+    Items items;
+    items.dense = ctot <= kDenseCap;
+    if (items.dense) {
+      const int base = warp_excl_scan(cnt, lane);
+      for (int j = 0; j < cnt; ++j) sm.dense[base + j] = sm.col[j][lane];
+      __syncwarp();
+      items.n = ctot;
+      items.n_it = (ctot + 31) >> 5;
+    } else {
+      items.n = cnt;
+      items.n_it = -warp_min_i(-cnt);
+    }
 
-    // ---- step 4: Gumbel race over the candidates
+    // ---- step 4: Gumbel race
     const uint32_t t32 = (uint32_t)t;
     const uint32_t ctr3 = a.iter_hi | (uint32_t)c;
     float loMax = -kInf, hiA = -kInf, hi2 = -kInf;
-    int iA = -1;
-    uint32_t xA = 0;
-    for (int i = lane; i < ctot; i += 32) {
-      const float2 it = Lb[i];
-      const uint32_t x = noise_word((uint32_t)__float_as_int(it.y), t32, cur.rid, ctr3, a.key0, a.key1);
+    float2 wA = make_float2(0.f, __int_as_float(-1));
+    for (int it = 0; it < items.n_it; ++it) {
+      float2 v;
+      if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
+      const uint32_t x = noise_word((uint32_t)__float_as_int(v.y), t32, cur.rid, ctr3, a.key0, a.key1);
       const float2 gb = gumbel_bounds(x);
-      const float lo = __fmaf_rn(tau, gb.x, it.x);
-      const float hi = __fmaf_rn(tau, gb.y, it.x);
-      loMax = fmaxf(loMax, lo);
-      if (iA < 0 || hi > hiA) {
+      const float2 sc2 = __ffma2_rn(make_float2(tau, tau), gb, make_float2(v.x, v.x));  // (lo, hi)
+      loMax = fmaxf(loMax, sc2.x);
+      if (sc2.y > hiA || __float_as_int(wA.y) < 0) {
         hi2 = hiA;
-        hiA = hi;
-        iA = i;
-        xA = x;
+        hiA = sc2.y;
+        wA = v;
       } else {
-        hi2 = fmaxf(hi2, hi);
+        hi2 = fmaxf(hi2, sc2.y);
       }
     }
     const float S = warp_max(loMax);
-    int w_item = -1;
+    float2 w = make_float2(0.f, __int_as_float(-1));
     bool exact = !(S > -kInf);
     if (!exact) {
       const float thr = S - (fabsf(S) + 1.f) * 0x1p-20f;
-      const bool cand = (iA >= 0) && (hiA >= thr);
+      const bool cand = (__float_as_int(wA.y) >= 0) && (hiA >= thr);
       const bool cplx = hi2 >= thr;
       const unsigned bc = __ballot_sync(0xffffffffu, cand);
       const bool anyc = __any_sync(0xffffffffu, cplx);
       if (__popc(bc) == 1 && !anyc) {
-        w_item = __shfl_sync(0xffffffffu, iA, __ffs(bc) - 1);
+        const int src = __ffs(bc) - 1;
+        w.x = __shfl_sync(0xffffffffu, wA.x, src);
+        w.y = __shfl_sync(0xffffffffu, wA.y, src);
       } else {
+        // exact G for the candidates the bounds cannot separate
         float bs = -kInf;
-        int bid = INT_MAX, bit = -1;
-        if (cplx) {
-          for (int i = lane; i < ctot; i += 32) {
-            const float2 it = Lb[i];
-            const int id = __float_as_int(it.y);
-            const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
-            const float hi = __fmaf_rn(tau, gumbel_bounds(x).y, it.x);
-            if (hi >= thr) {
-              const float sc = __fmaf_rn(tau, gumbel_accurate(x), it.x);
-              if (bit < 0 || sc > bs || (sc == bs && id < bid)) {
-                bs = sc;
-                bid = id;
-                bit = i;
-              }
+        int bid = INT_MAX;
+        float bz = 0.f;
+        for (int it = 0; it < items.n_it; ++it) {
+          float2 v;
+          if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
+          const int id = __float_as_int(v.y);
+          const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
+          const float hi = __fmaf_rn(tau, gumbel_bounds(x).y, v.x);
+          if (hi >= thr) {
+            const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
+            if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
+              bs = scr;
+              bid = id;
+              bz = v.x;
             }
           }
-        } else if (cand) {
-          const float2 it = Lb[iA];
-          bs = __fmaf_rn(tau, gumbel_accurate(xA), it.x);
-          bid = __float_as_int(it.y);
-          bit = iA;
         }
         const int wl = warp_argmax_lane(bs, bid);
-        w_item = __shfl_sync(0xffffffffu, bit, wl);
+        w.x = __shfl_sync(0xffffffffu, bz, wl);
+        w.y = __int_as_float(__shfl_sync(0xffffffffu, bid, wl));
       }
       // membership of the winner in the exact top-k (rank by (z desc, id asc))
       if (ctot > k) {
-        const float2 w = Lb[w_item];
         const int idw = __float_as_int(w.y);
         int rr = 0;
-        for (int i = lane; i < ctot; i += 32) {
-          const float2 it = Lb[i];
-          rr += (it.x > w.x || (it.x == w.x && __float_as_int(it.y) < idw)) ? 1 : 0;
+        for (int it = 0; it < items.n_it; ++it) {
+          float2 v;
+          if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
+          rr += (v.x > w.x || (v.x == w.x && __float_as_int(v.y) < idw)) ? 1 : 0;
         }
         if (warp_sum_i(rr) >= k) exact = true;
       }
     }
     if (exact) {
       // k-th largest composite key among the candidates (all keys distinct),
-      // one bit at a time from the top.
+      // one bit at a time from the top; every candidate is kept when ctot <= k.
       unsigned long long kth = 0ull;
-      for (int b = 63; b >= 0; --b) {
-        const unsigned long long probe = kth | (1ull << b);
-        int cb2 = 0;
-        for (int i = lane; i < ctot; i += 32) {
-          const float2 it = Lb[i];
-          cb2 += (rank_key(it.x, __float_as_int(it.y)) >= probe) ? 1 : 0;
+      if (ctot > k) {
+        for (int b = 63; b >= 0; --b) {
+          const unsigned long long probe = kth | (1ull << b);
+          int cb2 = 0;
+          for (int it = 0; it < items.n_it; ++it) {
+            float2 v;
+            if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
+            cb2 += (rank_key(v.x, __float_as_int(v.y)) >= probe) ? 1 : 0;
+          }
+          if (warp_sum_i(cb2) >= k) kth = probe;
         }
-        if (warp_sum_i(cb2) >= k) kth = probe;
       }
-      float bs = -kInf;
-      int bid = INT_MAX, bit = -1;
-      for (int i = lane; i < ctot; i += 32) {
-        const float2 it = Lb[i];
-        const int id = __float_as_int(it.y);
-        if (rank_key(it.x, id) >= kth) {
+      float bs = -kInf, bz = 0.f;
+      int bid = INT_MAX;
+      for (int it = 0; it < items.n_it; ++it) {
+        float2 v;
+        if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
+        const int id = __float_as_int(v.y);
+        if (rank_key(v.x, id) >= kth) {
           const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
-          const float sc = __fmaf_rn(tau, gumbel_accurate(x), it.x);
-          if (bit < 0 || sc > bs || (sc == bs && id < bid)) {
-            bs = sc;
+          const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
+          if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
+            bs = scr;
             bid = id;
-            bit = i;
+            bz = v.x;
           }
         }
       }
       const int wl = warp_argmax_lane(bs, bid);
-      w_item = __shfl_sync(0xffffffffu, bit, wl);
+      w.x = __shfl_sync(0xffffffffu, bz, wl);
+      w.y = __int_as_float(__shfl_sync(0xffffffffu, bid, wl));
     }
 
     // ---- step 5: output
     if (lane == 0) {
-      const float2 w = Lb[w_item];
       a.out_tokens[cell] = __float_as_int(w.y);
       a.out_logprobs[cell] = w.x - lse;
     }
@@ -384,35 +446,27 @@ __global__ void __launch_bounds__(kWarpKernelThreads) k_sample_warp(const Sample
 // ---------------------------------------------------------------- launcher
 template <int NCH>
 static cudaError_t launch_nch(const SampleArgs& a, cudaStream_t st, int num_sms) {
-  const size_t smem = (size_t)(kWarpKernelThreads / 32) * NCH * 256 * sizeof(float2);
-  static bool configured = false;  // per process; the attribute is per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_sample_warp<NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const size_t smem = (size_t)(kWarpKernelThreads / 32) * sizeof(WarpSmem<NCH>);
+  cudaError_t e = cudaFuncSetAttribute(k_sample_warp<NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_sample_warp<NCH>,
-                                                                kWarpKernelThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_sample_warp<NCH>, kWarpKernelThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const long long n_cells = (long long)a.C * a.P;
-  const long long warps_needed = n_cells;
   long long blocks = (long long)num_sms * per_sm;
-  const long long max_useful = (warps_needed + (kWarpKernelThreads / 32) - 1) / (kWarpKernelThreads / 32);
+  const long long max_useful = (n_cells + (kWarpKernelThreads / 32) - 1) / (kWarpKernelThreads / 32);
   if (blocks > max_useful) blocks = max_useful;
   if (blocks < 1) blocks = 1;
   k_sample_warp<NCH><<<(unsigned)blocks, kWarpKernelThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
-int warp_kernel_max_vocab() { return 8 * 256 - 7; }
+int warp_kernel_max_vocab() { return 8 * 256 + 7; }
 
 cudaError_t launch_sample_warp(const SampleArgs& a, cudaStream_t st, int num_sms) {
-  const int nq_max = (a.V + 7 + 7) >> 3;
-  const int nch = (nq_max + 31) / 32;
-  switch (nch) {
+  const int nch = ((a.V >> 3) + 31) / 32;
+  switch (nch < 1 ? 1 : nch) {
     case 1: return launch_nch<1>(a, st, num_sms);
     case 2: return launch_nch<2>(a, st, num_sms);
     case 3: return launch_nch<3>(a, st, num_sms);

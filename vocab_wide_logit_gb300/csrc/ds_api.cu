@@ -110,6 +110,11 @@ ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void
   a.key0 = (uint32_t)(seed & 0xffffffffull);
   a.key1 = (uint32_t)(seed >> 32);
   a.iter_hi = iteration << 8;
+  // Philox4x32-10 key schedule: round r uses key + r * (0x9E3779B9, 0xBB67AE85).
+  for (int r = 0; r < 10; ++r) {
+    a.rk0[r] = a.key0 + (uint32_t)r * 0x9E3779B9u;
+    a.rk1[r] = a.key1 + (uint32_t)r * 0xBB67AE85u;
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;

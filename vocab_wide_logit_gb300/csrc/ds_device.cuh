@@ -31,6 +31,7 @@ struct SampleArgs {
   float q_hi;         // N(0,1) quantile for the upper threshold (+inf: none)
   uint32_t key0, key1;
   uint32_t iter_hi;   // iteration << 8
+  uint32_t rk0[10], rk1[10];  // Philox round keys (key + r * Weyl constants), computed on the host
 };
 
 // ---------------------------------------------------------------- loads
@@ -73,27 +74,25 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 // ---------------------------------------------------------------- Philox4x32-10
 // Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3" (SC'11): each
-// round multiplies counter words 0 and 2 by two constants; the high halves are
-// xored with the other words and the round key, the low halves move over; the
-// key is bumped by two Weyl constants between rounds.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
+// round multiplies counter words 0 and 2 by two constants (32 x 32 -> 64 bits);
+// the high halves are xored with the other words and the round key, the low
+// halves move over. The round keys (the key bumped by two Weyl constants per
+// round) come precomputed in rk0 / rk1.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 x, const uint32_t (&rk0)[10], const uint32_t (&rk1)[10]) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t lo0 = 0xD2511F53u * x.x;
-    const uint32_t hi0 = __umulhi(0xD2511F53u, x.x);
-    const uint32_t lo1 = 0xCD9E8D57u * x.z;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, x.z);
-    x = make_uint4(hi1 ^ x.y ^ k0, lo1, hi0 ^ x.w ^ k1, lo0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+    const unsigned long long p0 = (unsigned long long)x.x * 0xD2511F53ull;
+    const unsigned long long p1 = (unsigned long long)x.z * 0xCD9E8D57ull;
+    x = make_uint4((uint32_t)(p1 >> 32) ^ x.y ^ rk0[r], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ x.w ^ rk1[r],
+                   (uint32_t)p0);
   }
   return x;
 }
 
 // Word (id & 3) of the Philox block keyed for vocabulary id `id` of a cell.
 __device__ __forceinline__ uint32_t noise_word(uint32_t id, uint32_t t, uint32_t rid, uint32_t ctr3,
-                                               uint32_t k0, uint32_t k1) {
-  const uint4 o = philox4x32_10(make_uint4(id >> 2, t, rid, ctr3), k0, k1);
+                                               const uint32_t (&rk0)[10], const uint32_t (&rk1)[10]) {
+  const uint4 o = philox4x32_10(make_uint4(id >> 2, t, rid, ctr3), rk0, rk1);
   const uint32_t s = id & 3u;
   const uint32_t a = (s & 1u) ? o.y : o.x;
   const uint32_t b = (s & 1u) ? o.w : o.z;

@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
         const int l = idxs[i];
         const float zi = zs[l];
         const int id = id_base + l;
-        const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
+        const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.rk0, a.rk1);
         const float2 sc2 = __ffma2_rn(tau2, gumbel_bounds(x), make_float2(zi, zi));
         loMax = fmaxf(loMax, sc2.x);
         top2_insert(tp, sc2.y, zi, id, x);
@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
           const int l = idxs[i];
           const float zi = zs[l];
           const int id = id_base + l;
-          const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
+          const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.rk0, a.rk1);
           if (__fmaf_rn(tau, gumbel_bounds(x).y, zi) >= thr) {
             const float scr = __fmaf_rn(tau, gumbel_accurate(x), zi);
             if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
@@ -629,7 +629,7 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
         const float zi = zs[l];
         const int id = id_base + l;
         if (rank_key(zi, id) >= kth) {
-          const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
+          const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.rk0, a.rk1);
           const float scr = __fmaf_rn(tau, gumbel_accurate(x), zi);
           if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
             bs = scr; bz = zi; bid = id;

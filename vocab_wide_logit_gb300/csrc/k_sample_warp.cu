@@ -36,6 +36,7 @@ template <int NCH>
 struct WarpSmem {
   float2 col[NCH * 8 + 1][32];  // per-lane candidate columns: (z, id as int bits)
   float2 dense[kDenseCap];      // balanced candidate list
+  int hist[256];                // radix histogram of the exact fallback
 };
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -64,7 +65,80 @@ struct Items {
   }
 };
 
-// Register budget per thread: 4 CTAs of 4 warps per SM up to NCH = 4.
+// Everything a warp needs to know about one cell before touching its logits.
+struct CellGeo {
+  int c, t;
+  float g, tau;
+  uint32_t rid;
+  uint32_t err;       // DS_DEV_ERR_* for this cell, 0 if fine
+  const uint16_t* crow;
+  const uint16_t* urow;
+  int h, nfc, ns, sid;
+  bool u_vec;         // u row aligned like the c row: vector loads
+};
+
+// Per-lane top-2 of the race by upper score bound, plus the largest bound of the rest.
+struct LaneTop2 {
+  float hA, hB, h3;
+  float2 vA, vB;  // (z, id bits)
+  uint32_t xA, xB;
+  __device__ __forceinline__ void init() {
+    hA = hB = h3 = -kInf;
+    vA = vB = make_float2(0.f, __int_as_float(-1));
+    xA = xB = 0u;
+  }
+  __device__ __forceinline__ void insert(float h, float2 v, uint32_t x) {
+    if (__float_as_int(vA.y) < 0 || h > hA) {
+      h3 = fmaxf(h3, hB);
+      hB = hA; vB = vA; xB = xA;
+      hA = h; vA = v; xA = x;
+    } else if (__float_as_int(vB.y) < 0 || h > hB) {
+      h3 = fmaxf(h3, hB);
+      hB = h; vB = v; xB = x;
+    } else {
+      h3 = fmaxf(h3, h);
+    }
+  }
+};
+
+template <int NCH>
+__device__ __forceinline__ void load_cell(const CellGeo& G, int lane, uint4 (&rc)[NCH], uint4 (&ru)[NCH],
+                                          uint32_t& sc, uint32_t& su) {
+  const uint4* cb = reinterpret_cast<const uint4*>(G.crow + G.h);
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int q = lane + 32 * j;
+    rc[j] = (q < G.nfc) ? ld_stream16(cb + q) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  sc = (lane < G.ns) ? (uint32_t)__ldg(G.crow + G.sid) : 0u;
+  su = 0u;
+  if (G.g != 0.f) {
+    if (G.u_vec) {
+      const uint4* ub = reinterpret_cast<const uint4*>(G.urow + G.h);
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const int q = lane + 32 * j;
+        ru[j] = (q < G.nfc) ? ld_stream16(ub + q) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else {
+      // u row aligned differently from the c row: gather element by element.
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const int q = lane + 32 * j;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (q < G.nfc) {
+          const uint16_t* src = G.urow + G.h + 8 * q;
+#pragma unroll
+          for (int hh = 0; hh < 4; ++hh)
+            w[hh] = (uint32_t)__ldg(src + 2 * hh) | ((uint32_t)__ldg(src + 2 * hh + 1) << 16);
+        }
+        ru[j] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    su = (lane < G.ns) ? (uint32_t)__ldg(G.urow + G.sid) : 0u;
+  }
+}
+
 template <int NCH>
 __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 6) ? 3 : 2))
     k_sample_warp(const SampleArgs a) {
@@ -93,13 +167,12 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
   const float2 neg1 = make_float2(-1.f, -1.f);
   const float2 l2e = make_float2(kLog2e, kLog2e);
 
+  // position -> request cursor over the warp's contiguous cell range
   ReqCursor cur;
   int c = (int)(cbeg / P);
   int p = (int)(cbeg - (long long)c * P);
   warp_find_request(a, p, lane, cur);
-
-  for (long long cell = cbeg; cell < cend; ++cell) {
-    // ---- position -> request (advance; restart at the next row)
+  auto next_geo = [&](long long cell) {
     if (p == P) {
       p = 0;
       ++c;
@@ -114,69 +187,61 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
       cur.tau = a.temperature[cur.r];
       cur.rid = (uint32_t)a.request_ids[cur.r];
     }
-    const int t = p - cur.off;
+    CellGeo G;
+    G.c = c;
+    G.t = p - cur.off;
     ++p;
-    const float g = cur.g, tau = cur.tau;
-    if (!(tau >= 0.f) || isnan(g) || (g != 0.f && a.u == nullptr)) {
+    G.g = cur.g;
+    G.tau = cur.tau;
+    G.rid = cur.rid;
+    G.err = (!(G.tau >= 0.f) || isnan(G.g)) ? DS_DEV_ERR_PARAM
+                                            : ((G.g != 0.f && a.u == nullptr) ? DS_DEV_ERR_NO_UNCOND : 0u);
+    G.crow = a.c + cell * (long long)V;
+    const uintptr_t ca = reinterpret_cast<uintptr_t>(G.crow);
+    G.h = min((int)(((16u - (unsigned)(ca & 15)) & 15u) >> 1), V);
+    G.nfc = (V - G.h) >> 3;
+    G.ns = V - 8 * G.nfc;
+    G.sid = (lane < G.h) ? lane : lane + 8 * G.nfc;
+    G.urow = nullptr;
+    G.u_vec = true;
+    if (G.err == 0u && G.g != 0.f) {
+      G.urow = a.u + ((long long)c * P_u + cur.off_u + G.t) * (long long)V;
+      G.u_vec = (reinterpret_cast<uintptr_t>(G.urow) & 15) == (ca & 15);
+    }
+    return G;
+  };
+
+  uint4 rc[NCH], ru[NCH];
+  uint32_t sc = 0u, su = 0u;
+  CellGeo nxt = next_geo(cbeg);
+  if (nxt.err == 0u) load_cell<NCH>(nxt, lane, rc, ru, sc, su);
+
+  for (long long cell = cbeg; cell < cend; ++cell) {
+    const CellGeo G = nxt;
+    const bool has_next = cell + 1 < cend;
+    auto prefetch_next = [&]() {
+      if (has_next) {
+        nxt = next_geo(cell + 1);
+        if (nxt.err == 0u) load_cell<NCH>(nxt, lane, rc, ru, sc, su);
+      }
+    };
+    if (G.err != 0u) {
       if (lane == 0) {
         a.out_tokens[cell] = -1;
         a.out_logprobs[cell] = __int_as_float(0x7fc00000);
-        report(a.d_status, (!(tau >= 0.f) || isnan(g)) ? DS_DEV_ERR_PARAM : DS_DEV_ERR_NO_UNCOND);
+        report(a.d_status, G.err);
       }
+      prefetch_next();
       continue;
     }
-
-    // ---- row geometry: h head elements, nfc aligned full chunks, ns scalar elements
-    const uint16_t* crow = a.c + cell * (long long)V;
-    const uintptr_t ca = reinterpret_cast<uintptr_t>(crow);
-    const int h = min((int)(((16u - (unsigned)(ca & 15)) & 15u) >> 1), V);
-    const int nfc = (V - h) >> 3;
-    const int ns = V - 8 * nfc;
-    const uint4* cb = reinterpret_cast<const uint4*>(ca + 2 * (uintptr_t)h);
-    const int sid = (lane < h) ? lane : lane + 8 * nfc;  // this lane's scalar element id (if lane < ns)
+    const float g = G.g, tau = G.tau;
     const bool guided = g != 0.f;
-
-    uint4 rc[NCH], ru[NCH];
-    uint32_t sc = 0, su = 0;
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int q = lane + 32 * j;
-      rc[j] = (q < nfc) ? ld_stream16(cb + q) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    if (lane < ns) sc = __ldg(crow + sid);
-    if (guided) {
-      const uint16_t* urow = a.u + ((long long)c * P_u + cur.off_u + t) * (long long)V;
-      const uintptr_t ua = reinterpret_cast<uintptr_t>(urow);
-      if ((ua & 15) == (ca & 15)) {
-        const uint4* ub = reinterpret_cast<const uint4*>(ua + 2 * (uintptr_t)h);
-#pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-          const int q = lane + 32 * j;
-          ru[j] = (q < nfc) ? ld_stream16(ub + q) : make_uint4(0u, 0u, 0u, 0u);
-        }
-      } else {
-        // u row aligned differently from the c row: gather element by element.
-#pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-          const int q = lane + 32 * j;
-          uint32_t w[4] = {0u, 0u, 0u, 0u};
-          if (q < nfc) {
-            const uint16_t* src = urow + h + 8 * q;
-#pragma unroll
-            for (int hh = 0; hh < 4; ++hh)
-              w[hh] = (uint32_t)__ldg(src + 2 * hh) | ((uint32_t)__ldg(src + 2 * hh + 1) << 16);
-          }
-          ru[j] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-      if (lane < ns) su = __ldg(urow + sid);
-    }
+    const int ns = G.ns, sid = G.sid;
 
     // ---- step 1: z, row max, moments of chunks 0..NCH-2 (always full)
     float2 z[NCH][4];
-    float zs1;
     const float2 g2 = make_float2(g, g);
-    float m = -kInf;
+    float m0 = -kInf, m1 = -kInf;
     float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
@@ -192,27 +257,31 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
           z[j][i] = cp;
         }
       }
-      if (j == NCH - 1 && !(lane + 32 * j < nfc)) {
+      if (j == NCH - 1 && !(lane + 32 * j < G.nfc)) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) z[j][i] = make_float2(-kInf, -kInf);
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) m = max3(m, z[j][i].x, z[j][i].y);
+      m0 = max3(m0, z[j][0].x, z[j][0].y);
+      m1 = max3(m1, z[j][1].x, z[j][1].y);
+      m0 = max3(m0, z[j][2].x, z[j][2].y);
+      m1 = max3(m1, z[j][3].x, z[j][3].y);
       if (j < NCH - 1) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          s1 = __fadd2_rn(s1, z[j][i]);
-          s2 = __ffma2_rn(z[j][i], z[j][i], s2);
-        }
+        s1 = __fadd2_rn(s1, __fadd2_rn(z[j][0], z[j][1]));
+        s1 = __fadd2_rn(s1, __fadd2_rn(z[j][2], z[j][3]));
+        s2 = __ffma2_rn(z[j][0], z[j][0], s2);
+        s2 = __ffma2_rn(z[j][1], z[j][1], s2);
+        s2 = __ffma2_rn(z[j][2], z[j][2], s2);
+        s2 = __ffma2_rn(z[j][3], z[j][3], s2);
       }
     }
+    float zs1;
     {
       const float cf = __uint_as_float(sc << 16);
       zs1 = (lane < ns) ? (guided ? cfg_combine(cf, __uint_as_float(su << 16), g) : cf) : -kInf;
-      m = fmaxf(m, zs1);
     }
-    m = warp_max(m);
+    const float m = warp_max(max3(m0, m1, zs1));
     if (m == -kInf) {  // every logit is -inf: token 0, logprob NaN
+      prefetch_next();
       if (lane == 0) {
         a.out_tokens[cell] = 0;
         a.out_logprobs[cell] = __int_as_float(0x7fc00000);
@@ -220,27 +289,31 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
       continue;
     }
     const float2 nml = make_float2(-m * kLog2e, -m * kLog2e);
-    const int idb = h + 8 * lane;  // id of element (j, 0) is idb + 256 j
+    const int idb = G.h + 8 * lane;  // id of element (j, 0) is idb + 256 j
 
     // ---- tau == 0: logsumexp and the smallest id attaining the max
     if (!(tau > 0.f)) {
-      float2 acc = make_float2(0.f, 0.f);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
       int am = INT_MAX;
 #pragma unroll
       for (int j = NCH - 1; j >= 0; --j) {
 #pragma unroll
         for (int i = 3; i >= 0; --i) {
           const float2 tt = __ffma2_rn(z[j][i], l2e, nml);
-          acc = __fadd2_rn(acc, make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
+          if (i & 1)
+            acc1 = __fadd2_rn(acc1, make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
+          else
+            acc0 = __fadd2_rn(acc0, make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
           if (z[j][i].y == m) am = idb + 256 * j + 2 * i + 1;
           if (z[j][i].x == m) am = idb + 256 * j + 2 * i;
         }
       }
-      float ssum = acc.x + acc.y;
+      float ssum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
       if (lane < ns) {
         ssum += ex2_approx((zs1 - m) * kLog2e);
         if (zs1 == m) am = min(am, sid);
       }
+      prefetch_next();
       const float lse = m + logf(warp_sum(ssum));
       am = warp_min_i(am);
       if (lane == 0) {
@@ -251,13 +324,13 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
     }
 
     // ---- threshold guess from the subsample moments
-    float mu = 0.f, sd = 0.f, tlo = -FLT_MAX;  // -FLT_MAX: keep every finite element
+    float tlo = -FLT_MAX;  // -FLT_MAX: keep every finite element
     bool guessed = false;
     if (NCH >= 2 && a.q_lo > -kInf) {
       const float n_s = (float)(32 * 8 * (NCH > 1 ? NCH - 1 : 1));
       const float S1 = warp_sum(s1.x + s1.y), S2 = warp_sum(s2.x + s2.y);
-      mu = S1 / n_s;
-      sd = sqrtf(fmaxf(S2 / n_s - mu * mu, 0.f));
+      const float mu = S1 / n_s;
+      const float sd = sqrtf(fmaxf(S2 / n_s - mu * mu, 0.f));
       const float guess = fmaf(sd, a.q_lo, mu);
       if (isfinite(guess)) {
         tlo = fminf(guess, m);
@@ -267,14 +340,17 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
 
     // ---- step 2: logsumexp and speculative compaction of z >= t_lo into this lane's column
     float2* colp = &sm.col[0][lane];
-    float2 acc = make_float2(0.f, 0.f);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 zz = z[j][i];
         const float2 tt = __ffma2_rn(zz, l2e, nml);
-        acc = __fadd2_rn(acc, make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
+        if (i & 1)
+          acc1 = __fadd2_rn(acc1, make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
+        else
+          acc0 = __fadd2_rn(acc0, make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
         const int id0 = idb + 256 * j + 2 * i;
         *colp = make_float2(zz.x, __int_as_float(id0));
         colp += (zz.x >= tlo) ? 32 : 0;
@@ -282,13 +358,12 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
         colp += (zz.y >= tlo) ? 32 : 0;
       }
     }
-    float ssum = acc.x + acc.y;
+    float ssum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
     if (lane < ns) {
       ssum += ex2_approx((zs1 - m) * kLog2e);
       *colp = make_float2(zs1, __int_as_float(sid));
       colp += (zs1 >= tlo) ? 32 : 0;
     }
-    const float lse = m + logf(warp_sum(ssum));
     int cnt = (int)(colp - &sm.col[0][lane]) >> 5;
     int ctot = warp_sum_i(cnt);
 
@@ -314,6 +389,9 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
       cnt = (int)(colp - &sm.col[0][lane]) >> 5;
       ctot = warp_sum_i(cnt);
     }
+    // z is dead from here on: start loading the next cell while this one races
+    prefetch_next();
+    const float lse = m + logf(warp_sum(ssum));
     __syncwarp();
     Items items;
     items.dense = ctot <= kDenseCap;
@@ -328,24 +406,29 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
       items.n_it = -warp_min_i(-cnt);
     }
 
-    // ---- step 4: Gumbel race
-    const uint32_t t32 = (uint32_t)t;
-    const uint32_t ctr3 = a.iter_hi | (uint32_t)c;
-    float loMax = -kInf, hiA = -kInf, hi2 = -kInf;
-    float2 wA = make_float2(0.f, __int_as_float(-1));
-    for (int it = 0; it < items.n_it; ++it) {
-      float2 v;
-      if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
-      const uint32_t x = noise_word((uint32_t)__float_as_int(v.y), t32, cur.rid, ctr3, a.key0, a.key1);
-      const float2 gb = gumbel_bounds(x);
-      const float2 sc2 = __ffma2_rn(make_float2(tau, tau), gb, make_float2(v.x, v.x));  // (lo, hi)
-      loMax = fmaxf(loMax, sc2.x);
-      if (sc2.y > hiA || __float_as_int(wA.y) < 0) {
-        hi2 = hiA;
-        hiA = sc2.y;
-        wA = v;
-      } else {
-        hi2 = fmaxf(hi2, sc2.y);
+    // ---- step 4: Gumbel race, two candidates per iteration
+    const uint32_t t32 = (uint32_t)G.t;
+    const uint32_t ctr3 = a.iter_hi | (uint32_t)G.c;
+    const uint32_t rid = G.rid;
+    const float2 tau2 = make_float2(tau, tau);
+    float loMax = -kInf;
+    LaneTop2 tp;
+    tp.init();
+    for (int it = 0; it < items.n_it; it += 2) {
+      float2 v0, v1;
+      const bool ok0 = items.get(sm.col, sm.dense, it, lane, v0);
+      const bool ok1 = items.get(sm.col, sm.dense, it + 1, lane, v1);
+      if (!ok0) continue;
+      const uint32_t x0 = noise_word((uint32_t)__float_as_int(v0.y), t32, rid, ctr3, a.rk0, a.rk1);
+      uint32_t x1 = 0u;
+      if (ok1) x1 = noise_word((uint32_t)__float_as_int(v1.y), t32, rid, ctr3, a.rk0, a.rk1);
+      const float2 sc0 = __ffma2_rn(tau2, gumbel_bounds(x0), make_float2(v0.x, v0.x));  // (lo, hi)
+      loMax = fmaxf(loMax, sc0.x);
+      tp.insert(sc0.y, v0, x0);
+      if (ok1) {
+        const float2 sc1 = __ffma2_rn(tau2, gumbel_bounds(x1), make_float2(v1.x, v1.x));
+        loMax = fmaxf(loMax, sc1.x);
+        tp.insert(sc1.y, v1, x1);
       }
     }
     const float S = warp_max(loMax);
@@ -353,33 +436,39 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
     bool exact = !(S > -kInf);
     if (!exact) {
       const float thr = S - (fabsf(S) + 1.f) * 0x1p-20f;
-      const bool cand = (__float_as_int(wA.y) >= 0) && (hiA >= thr);
-      const bool cplx = hi2 >= thr;
-      const unsigned bc = __ballot_sync(0xffffffffu, cand);
+      const bool cA = (__float_as_int(tp.vA.y) >= 0) && (tp.hA >= thr);
+      const bool cB = (__float_as_int(tp.vB.y) >= 0) && (tp.hB >= thr);
+      const bool cplx = tp.h3 >= thr;
+      const unsigned bA = __ballot_sync(0xffffffffu, cA);
+      const unsigned bB = __ballot_sync(0xffffffffu, cB);
       const bool anyc = __any_sync(0xffffffffu, cplx);
-      if (__popc(bc) == 1 && !anyc) {
-        const int src = __ffs(bc) - 1;
-        w.x = __shfl_sync(0xffffffffu, wA.x, src);
-        w.y = __shfl_sync(0xffffffffu, wA.y, src);
+      if (__popc(bA) + __popc(bB) == 1 && !anyc) {
+        const int src = __ffs(bA) - 1;  // the single candidate is some lane's A
+        w.x = __shfl_sync(0xffffffffu, tp.vA.x, src);
+        w.y = __shfl_sync(0xffffffffu, tp.vA.y, src);
       } else {
         // exact G for the candidates the bounds cannot separate
-        float bs = -kInf;
+        float bs = -kInf, bz = 0.f;
         int bid = INT_MAX;
-        float bz = 0.f;
-        for (int it = 0; it < items.n_it; ++it) {
-          float2 v;
-          if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
+        auto consider = [&](float2 v, uint32_t x) {
           const int id = __float_as_int(v.y);
-          const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
-          const float hi = __fmaf_rn(tau, gumbel_bounds(x).y, v.x);
-          if (hi >= thr) {
-            const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
-            if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
-              bs = scr;
-              bid = id;
-              bz = v.x;
-            }
+          const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
+          if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
+            bs = scr;
+            bid = id;
+            bz = v.x;
           }
+        };
+        if (cplx) {
+          for (int it = 0; it < items.n_it; ++it) {
+            float2 v;
+            if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
+            const uint32_t x = noise_word((uint32_t)__float_as_int(v.y), t32, rid, ctr3, a.rk0, a.rk1);
+            if (__fmaf_rn(tau, gumbel_bounds(x).y, v.x) >= thr) consider(v, x);
+          }
+        } else {
+          if (cA) consider(tp.vA, tp.xA);
+          if (cB) consider(tp.vB, tp.xB);
         }
         const int wl = warp_argmax_lane(bs, bid);
         w.x = __shfl_sync(0xffffffffu, bz, wl);
@@ -398,19 +487,51 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
       }
     }
     if (exact) {
-      // k-th largest composite key among the candidates (all keys distinct),
-      // one bit at a time from the top; every candidate is kept when ctot <= k.
+      // Exact kept set: the k-th largest composite key (z desc, id asc) among the
+      // candidates, by an 8-bit radix select over shared-memory histograms; every
+      // candidate is kept when ctot <= k.
       unsigned long long kth = 0ull;
       if (ctot > k) {
-        for (int b = 63; b >= 0; --b) {
-          const unsigned long long probe = kth | (1ull << b);
-          int cb2 = 0;
+        int need = k;
+        for (int shift = 56; shift >= 0; shift -= 8) {
+          for (int b = lane; b < 256; b += 32) sm.hist[b] = 0;
+          __syncwarp();
           for (int it = 0; it < items.n_it; ++it) {
             float2 v;
             if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
-            cb2 += (rank_key(v.x, __float_as_int(v.y)) >= probe) ? 1 : 0;
+            const unsigned long long key = rank_key(v.x, __float_as_int(v.y));
+            const bool match = (shift == 56) || ((key >> (shift + 8)) == (kth >> (shift + 8)));
+            if (match) atomicAdd(&sm.hist[(int)((key >> shift) & 255ull)], 1);
           }
-          if (warp_sum_i(cb2) >= k) kth = probe;
+          __syncwarp();
+          // bins in descending digit order: lane l holds digits 255-8l .. 248-8l
+          int cl[8], tot = 0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            cl[e] = sm.hist[255 - 8 * lane - e];
+            tot += cl[e];
+          }
+          const int above_lane = warp_excl_scan(tot, lane);
+          const bool here = above_lane < need && need <= above_lane + tot;
+          const int src = __ffs(__ballot_sync(0xffffffffu, here)) - 1;
+          int digit = 0, above = 0;
+          if (lane == src) {
+            int run = above_lane;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              if (run + cl[e] >= need) {
+                digit = 255 - 8 * lane - e;
+                above = run;
+                break;
+              }
+              run += cl[e];
+            }
+          }
+          digit = __shfl_sync(0xffffffffu, digit, src);
+          above = __shfl_sync(0xffffffffu, above, src);
+          kth |= (unsigned long long)digit << shift;
+          need -= above;
+          __syncwarp();
         }
       }
       float bs = -kInf, bz = 0.f;
@@ -420,7 +541,7 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
         if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
         const int id = __float_as_int(v.y);
         if (rank_key(v.x, id) >= kth) {
-          const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.key0, a.key1);
+          const uint32_t x = noise_word((uint32_t)id, t32, rid, ctr3, a.rk0, a.rk1);
           const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
           if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
             bs = scr;

@@ -45,6 +45,11 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
+// (z, id) pair stored at a 32-bit shared-memory address.
+__device__ __forceinline__ void st_pair(uint32_t addr, float z, int id) {
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(z), "f"(__int_as_float(id)) : "memory");
+}
+
 // Iterates over this lane's share of the candidates: a balanced slice of the
 // dense list, or (when it overflowed) the lane's own column.
 struct Items {
@@ -77,29 +82,204 @@ struct CellGeo {
   bool u_vec;         // u row aligned like the c row: vector loads
 };
 
-// Per-lane top-2 of the race by upper score bound, plus the largest bound of the rest.
-struct LaneTop2 {
-  float hA, hB, h3;
-  float2 vA, vB;  // (z, id bits)
-  uint32_t xA, xB;
-  __device__ __forceinline__ void init() {
-    hA = hB = h3 = -kInf;
-    vA = vB = make_float2(0.f, __int_as_float(-1));
-    xA = xB = 0u;
+
+// k-th largest composite key (z desc, id asc) among n candidates read through
+// get(i), by an 8-bit radix select over a shared-memory histogram (keys are
+// distinct, so exactly one candidate holds it).
+template <typename Get>
+__device__ __noinline__ unsigned long long kth_key(Get get, int n_it, int k, int lane, int* hist) {
+  unsigned long long kth = 0ull;
+  int need = k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int b = lane; b < 256; b += 32) hist[b] = 0;
+    __syncwarp();
+    for (int it = 0; it < n_it; ++it) {
+      float2 v;
+      if (!get(it, v)) continue;
+      const unsigned long long key = rank_key(v.x, __float_as_int(v.y));
+      const bool match = (shift == 56) || ((key >> (shift + 8)) == (kth >> (shift + 8)));
+      if (match) atomicAdd(&hist[(int)((key >> shift) & 255ull)], 1);
+    }
+    __syncwarp();
+    // bins in descending digit order: lane l holds digits 255-8l .. 248-8l
+    int cl[8], tot = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      cl[e] = hist[255 - 8 * lane - e];
+      tot += cl[e];
+    }
+    const int above_lane = warp_excl_scan(tot, lane);
+    const bool here = above_lane < need && need <= above_lane + tot;
+    const int src = __ffs(__ballot_sync(0xffffffffu, here)) - 1;
+    int digit = 0, above = 0;
+    if (lane == src) {
+      int run = above_lane;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (run + cl[e] >= need) {
+          digit = 255 - 8 * lane - e;
+          above = run;
+          break;
+        }
+        run += cl[e];
+      }
+    }
+    digit = __shfl_sync(0xffffffffu, digit, src);
+    above = __shfl_sync(0xffffffffu, above, src);
+    kth |= (unsigned long long)digit << shift;
+    need -= above;
+    __syncwarp();
   }
-  __device__ __forceinline__ void insert(float h, float2 v, uint32_t x) {
-    if (__float_as_int(vA.y) < 0 || h > hA) {
-      h3 = fmaxf(h3, hB);
-      hB = hA; vB = vA; xB = xA;
-      hA = h; vA = v; xA = x;
-    } else if (__float_as_int(vB.y) < 0 || h > hB) {
-      h3 = fmaxf(h3, hB);
-      hB = h; vB = v; xB = x;
-    } else {
-      h3 = fmaxf(h3, h);
+  return kth;
+}
+
+// Exact race over the candidates at or above key kth: G evaluated exactly for every one.
+template <typename Get>
+__device__ __noinline__ float2 race_exact(const SampleArgs& a, Get get, int n_it, unsigned long long kth, float tau,
+                                          uint32_t t32, uint32_t rid, uint32_t ctr3) {
+  float bs = -kInf, bz = 0.f;
+  int bid = INT_MAX;
+  for (int it = 0; it < n_it; ++it) {
+    float2 v;
+    if (!get(it, v)) continue;
+    const int id = __float_as_int(v.y);
+    if (rank_key(v.x, id) >= kth) {
+      const uint32_t x = noise_word((uint32_t)id, t32, rid, ctr3, a.rk0, a.rk1);
+      const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
+      if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
+        bs = scr;
+        bid = id;
+        bz = v.x;
+      }
     }
   }
-};
+  const int wl = warp_argmax_lane(bs, bid);
+  return make_float2(__shfl_sync(0xffffffffu, bz, wl), __int_as_float(__shfl_sync(0xffffffffu, bid, wl)));
+}
+
+// Exact G for the candidates whose upper bound reaches thr, then the argmax.
+template <typename Get>
+__device__ __noinline__ float2 race_resolve(const SampleArgs& a, Get get, int n_it, float thr, float tau,
+                                            uint32_t t32, uint32_t rid, uint32_t ctr3) {
+  float bs = -kInf, bz = 0.f;
+  int bid = INT_MAX;
+  for (int it = 0; it < n_it; ++it) {
+    float2 v;
+    if (!get(it, v)) continue;
+    const int id = __float_as_int(v.y);
+    const uint32_t x = noise_word((uint32_t)id, t32, rid, ctr3, a.rk0, a.rk1);
+    if (__fmaf_rn(tau, gumbel_bounds(x).y, v.x) >= thr) {
+      const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
+      if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
+        bs = scr;
+        bid = id;
+        bz = v.x;
+      }
+    }
+  }
+  const int wl = warp_argmax_lane(bs, bid);
+  return make_float2(__shfl_sync(0xffffffffu, bz, wl), __int_as_float(__shfl_sync(0xffffffffu, bid, wl)));
+}
+
+// Rank of (zw, idw) among the candidates: how many precede it in (z desc, id asc).
+template <typename Get>
+__device__ __forceinline__ int rank_of(Get get, int n_it, float zw, int idw) {
+  int rr = 0;
+  for (int it = 0; it < n_it; ++it) {
+    float2 v;
+    if (!get(it, v)) continue;
+    rr += (v.x > zw || (v.x == zw && __float_as_int(v.y) < idw)) ? 1 : 0;
+  }
+  return warp_sum_i(rr);
+}
+
+// The race over a balanced candidate list (the common case): table bounds for
+// two candidates per lane and iteration, branch-free top-2 by upper bound.
+__device__ __forceinline__ float2 race_dense(const SampleArgs& a, const float2* dense, int ctot, int k, float tau,
+                                             uint32_t t32, uint32_t rid, uint32_t ctr3, int lane, int* hist) {
+  const float2 tau2 = make_float2(tau, tau);
+  float loMax = -kInf, hA = -kInf, hB = -kInf;
+  int iA = 0;
+  for (int base = 0; base < ctot; base += 64) {
+    const int i0 = base + lane, i1 = i0 + 32;
+    const bool ok0 = i0 < ctot, ok1 = i1 < ctot;
+    const float2 v0 = dense[ok0 ? i0 : 0];
+    const float2 v1 = dense[ok1 ? i1 : 0];
+    const uint32_t x0 = noise_word(__float_as_uint(v0.y), t32, rid, ctr3, a.rk0, a.rk1);
+    const uint32_t x1 = noise_word(__float_as_uint(v1.y), t32, rid, ctr3, a.rk0, a.rk1);
+    float2 s0 = __ffma2_rn(tau2, gumbel_bounds(x0), make_float2(v0.x, v0.x));  // (lower, upper) score
+    float2 s1 = __ffma2_rn(tau2, gumbel_bounds(x1), make_float2(v1.x, v1.x));
+    s0 = ok0 ? s0 : make_float2(-kInf, -kInf);
+    s1 = ok1 ? s1 : make_float2(-kInf, -kInf);
+    loMax = fmaxf(loMax, fmaxf(s0.x, s1.x));
+    bool gt = s0.y > hA;
+    hB = gt ? hA : fmaxf(hB, s0.y);
+    iA = gt ? i0 : iA;
+    hA = fmaxf(hA, s0.y);
+    gt = s1.y > hA;
+    hB = gt ? hA : fmaxf(hB, s1.y);
+    iA = gt ? i1 : iA;
+    hA = fmaxf(hA, s1.y);
+  }
+  auto get = [&](int it, float2& v) {
+    const int i = lane + 32 * it;
+    if (i >= ctot) return false;
+    v = dense[i];
+    return true;
+  };
+  const int n_it = (ctot + 31) >> 5;
+  const float S = warp_max(loMax);
+  float2 w;
+  bool exact = !(S > -kInf);
+  if (!exact) {
+    const float thr = S - (fabsf(S) + 1.f) * 0x1p-20f;
+    const unsigned bc = __ballot_sync(0xffffffffu, hA >= thr);
+    const bool cplx = __any_sync(0xffffffffu, hB >= thr);
+    if (__popc(bc) == 1 && !cplx) {
+      w = dense[__shfl_sync(0xffffffffu, iA, __ffs(bc) - 1)];
+    } else {
+      w = race_resolve(a, get, n_it, thr, tau, t32, rid, ctr3);
+    }
+    // membership of the winner in the exact top-k
+    if (ctot > k && rank_of(get, n_it, w.x, __float_as_int(w.y)) >= k) exact = true;
+  }
+  if (exact) {
+    const unsigned long long kth = (ctot > k) ? kth_key(get, n_it, k, lane, hist) : 0ull;
+    w = race_exact(a, get, n_it, kth, tau, t32, rid, ctr3);
+  }
+  return w;
+}
+
+// The race over per-lane candidate columns (when too many candidates for the
+// balanced list): every step walks the lane's own column.
+template <int NCH>
+__device__ __noinline__ float2 race_generic(const SampleArgs& a, WarpSmem<NCH>& sm, const Items& items, int ctot,
+                                            int k, float tau, uint32_t t32, uint32_t rid, uint32_t ctr3, int lane) {
+  auto get = [&](int it, float2& v) { return items.get(sm.col, sm.dense, it, lane, v); };
+  float loMax = -kInf, hA = -kInf, hB = -kInf;
+  for (int it = 0; it < items.n_it; ++it) {
+    float2 v;
+    if (!get(it, v)) continue;
+    const uint32_t x = noise_word(__float_as_uint(v.y), t32, rid, ctr3, a.rk0, a.rk1);
+    const float2 sc = __ffma2_rn(make_float2(tau, tau), gumbel_bounds(x), make_float2(v.x, v.x));
+    loMax = fmaxf(loMax, sc.x);
+    hB = (sc.y > hA) ? hA : fmaxf(hB, sc.y);
+    hA = fmaxf(hA, sc.y);
+  }
+  const float S = warp_max(loMax);
+  float2 w = make_float2(0.f, 0.f);
+  bool exact = !(S > -kInf);
+  if (!exact) {
+    const float thr = S - (fabsf(S) + 1.f) * 0x1p-20f;
+    w = race_resolve(a, get, items.n_it, thr, tau, t32, rid, ctr3);
+    if (ctot > k && rank_of(get, items.n_it, w.x, __float_as_int(w.y)) >= k) exact = true;
+  }
+  if (exact) {
+    const unsigned long long kth = (ctot > k) ? kth_key(get, items.n_it, k, lane, sm.hist) : 0ull;
+    w = race_exact(a, get, items.n_it, kth, tau, t32, rid, ctr3);
+  }
+  return w;
+}
 
 template <int NCH>
 __device__ __forceinline__ void load_cell(const CellGeo& G, int lane, uint4 (&rc)[NCH], uint4 (&ru)[NCH],
@@ -327,10 +507,10 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
     float tlo = -FLT_MAX;  // -FLT_MAX: keep every finite element
     bool guessed = false;
     if (NCH >= 2 && a.q_lo > -kInf) {
-      const float n_s = (float)(32 * 8 * (NCH > 1 ? NCH - 1 : 1));
+      const float inv_n = 1.0f / (float)(32 * 8 * (NCH > 1 ? NCH - 1 : 1));  // power of two: exact
       const float S1 = warp_sum(s1.x + s1.y), S2 = warp_sum(s2.x + s2.y);
-      const float mu = S1 / n_s;
-      const float sd = sqrtf(fmaxf(S2 / n_s - mu * mu, 0.f));
+      const float mu = S1 * inv_n;
+      const float sd = sqrtf(fmaxf(fmaf(S2, inv_n, -mu * mu), 0.f));
       const float guess = fmaf(sd, a.q_lo, mu);
       if (isfinite(guess)) {
         tlo = fminf(guess, m);
@@ -339,7 +519,10 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
     }
 
     // ---- step 2: logsumexp and speculative compaction of z >= t_lo into this lane's column
-    float2* colp = &sm.col[0][lane];
+    // (the store is unconditional; the column address advances by one row only
+    // for kept elements, so the lane's last store lands in an unused row)
+    const uint32_t col0 = (uint32_t)__cvta_generic_to_shared(&sm.col[0][lane]);
+    uint32_t ca = col0;
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
@@ -352,41 +535,37 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
         else
           acc0 = __fadd2_rn(acc0, make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
         const int id0 = idb + 256 * j + 2 * i;
-        *colp = make_float2(zz.x, __int_as_float(id0));
-        colp += (zz.x >= tlo) ? 32 : 0;
-        *colp = make_float2(zz.y, __int_as_float(id0 + 1));
-        colp += (zz.y >= tlo) ? 32 : 0;
+        st_pair(ca, zz.x, id0);
+        ca += (zz.x >= tlo) ? 256u : 0u;
+        st_pair(ca, zz.y, id0 + 1);
+        ca += (zz.y >= tlo) ? 256u : 0u;
       }
     }
     float ssum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
-    if (lane < ns) {
-      ssum += ex2_approx((zs1 - m) * kLog2e);
-      *colp = make_float2(zs1, __int_as_float(sid));
-      colp += (zs1 >= tlo) ? 32 : 0;
-    }
-    int cnt = (int)(colp - &sm.col[0][lane]) >> 5;
+    ssum += (lane < ns) ? ex2_approx((zs1 - m) * kLog2e) : 0.f;
+    st_pair(ca, zs1, sid);
+    ca += (zs1 >= tlo) ? 256u : 0u;  // zs1 is -inf for lanes without a scalar element
+    int cnt = (int)((ca - col0) >> 8);
     int ctot = warp_sum_i(cnt);
 
     // ---- step 3: the guess must cover the top k; otherwise keep every finite element
     if (guessed && ctot < k) {
       tlo = -FLT_MAX;
-      colp = &sm.col[0][lane];
+      ca = col0;
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int id0 = idb + 256 * j + 2 * i;
-          *colp = make_float2(z[j][i].x, __int_as_float(id0));
-          colp += (z[j][i].x >= tlo) ? 32 : 0;
-          *colp = make_float2(z[j][i].y, __int_as_float(id0 + 1));
-          colp += (z[j][i].y >= tlo) ? 32 : 0;
+          st_pair(ca, z[j][i].x, id0);
+          ca += (z[j][i].x >= tlo) ? 256u : 0u;
+          st_pair(ca, z[j][i].y, id0 + 1);
+          ca += (z[j][i].y >= tlo) ? 256u : 0u;
         }
       }
-      if (lane < ns) {
-        *colp = make_float2(zs1, __int_as_float(sid));
-        colp += (zs1 >= tlo) ? 32 : 0;
-      }
-      cnt = (int)(colp - &sm.col[0][lane]) >> 5;
+      st_pair(ca, zs1, sid);
+      ca += (zs1 >= tlo) ? 256u : 0u;
+      cnt = (int)((ca - col0) >> 8);
       ctot = warp_sum_i(cnt);
     }
     // z is dead from here on: start loading the next cell while this one races
@@ -406,153 +585,15 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
       items.n_it = -warp_min_i(-cnt);
     }
 
-    // ---- step 4: Gumbel race, two candidates per iteration
+    // ---- step 4: Gumbel race
     const uint32_t t32 = (uint32_t)G.t;
     const uint32_t ctr3 = a.iter_hi | (uint32_t)G.c;
     const uint32_t rid = G.rid;
-    const float2 tau2 = make_float2(tau, tau);
-    float loMax = -kInf;
-    LaneTop2 tp;
-    tp.init();
-    for (int it = 0; it < items.n_it; it += 2) {
-      float2 v0, v1;
-      const bool ok0 = items.get(sm.col, sm.dense, it, lane, v0);
-      const bool ok1 = items.get(sm.col, sm.dense, it + 1, lane, v1);
-      if (!ok0) continue;
-      const uint32_t x0 = noise_word((uint32_t)__float_as_int(v0.y), t32, rid, ctr3, a.rk0, a.rk1);
-      uint32_t x1 = 0u;
-      if (ok1) x1 = noise_word((uint32_t)__float_as_int(v1.y), t32, rid, ctr3, a.rk0, a.rk1);
-      const float2 sc0 = __ffma2_rn(tau2, gumbel_bounds(x0), make_float2(v0.x, v0.x));  // (lo, hi)
-      loMax = fmaxf(loMax, sc0.x);
-      tp.insert(sc0.y, v0, x0);
-      if (ok1) {
-        const float2 sc1 = __ffma2_rn(tau2, gumbel_bounds(x1), make_float2(v1.x, v1.x));
-        loMax = fmaxf(loMax, sc1.x);
-        tp.insert(sc1.y, v1, x1);
-      }
-    }
-    const float S = warp_max(loMax);
-    float2 w = make_float2(0.f, __int_as_float(-1));
-    bool exact = !(S > -kInf);
-    if (!exact) {
-      const float thr = S - (fabsf(S) + 1.f) * 0x1p-20f;
-      const bool cA = (__float_as_int(tp.vA.y) >= 0) && (tp.hA >= thr);
-      const bool cB = (__float_as_int(tp.vB.y) >= 0) && (tp.hB >= thr);
-      const bool cplx = tp.h3 >= thr;
-      const unsigned bA = __ballot_sync(0xffffffffu, cA);
-      const unsigned bB = __ballot_sync(0xffffffffu, cB);
-      const bool anyc = __any_sync(0xffffffffu, cplx);
-      if (__popc(bA) + __popc(bB) == 1 && !anyc) {
-        const int src = __ffs(bA) - 1;  // the single candidate is some lane's A
-        w.x = __shfl_sync(0xffffffffu, tp.vA.x, src);
-        w.y = __shfl_sync(0xffffffffu, tp.vA.y, src);
-      } else {
-        // exact G for the candidates the bounds cannot separate
-        float bs = -kInf, bz = 0.f;
-        int bid = INT_MAX;
-        auto consider = [&](float2 v, uint32_t x) {
-          const int id = __float_as_int(v.y);
-          const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
-          if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
-            bs = scr;
-            bid = id;
-            bz = v.x;
-          }
-        };
-        if (cplx) {
-          for (int it = 0; it < items.n_it; ++it) {
-            float2 v;
-            if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
-            const uint32_t x = noise_word((uint32_t)__float_as_int(v.y), t32, rid, ctr3, a.rk0, a.rk1);
-            if (__fmaf_rn(tau, gumbel_bounds(x).y, v.x) >= thr) consider(v, x);
-          }
-        } else {
-          if (cA) consider(tp.vA, tp.xA);
-          if (cB) consider(tp.vB, tp.xB);
-        }
-        const int wl = warp_argmax_lane(bs, bid);
-        w.x = __shfl_sync(0xffffffffu, bz, wl);
-        w.y = __int_as_float(__shfl_sync(0xffffffffu, bid, wl));
-      }
-      // membership of the winner in the exact top-k (rank by (z desc, id asc))
-      if (ctot > k) {
-        const int idw = __float_as_int(w.y);
-        int rr = 0;
-        for (int it = 0; it < items.n_it; ++it) {
-          float2 v;
-          if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
-          rr += (v.x > w.x || (v.x == w.x && __float_as_int(v.y) < idw)) ? 1 : 0;
-        }
-        if (warp_sum_i(rr) >= k) exact = true;
-      }
-    }
-    if (exact) {
-      // Exact kept set: the k-th largest composite key (z desc, id asc) among the
-      // candidates, by an 8-bit radix select over shared-memory histograms; every
-      // candidate is kept when ctot <= k.
-      unsigned long long kth = 0ull;
-      if (ctot > k) {
-        int need = k;
-        for (int shift = 56; shift >= 0; shift -= 8) {
-          for (int b = lane; b < 256; b += 32) sm.hist[b] = 0;
-          __syncwarp();
-          for (int it = 0; it < items.n_it; ++it) {
-            float2 v;
-            if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
-            const unsigned long long key = rank_key(v.x, __float_as_int(v.y));
-            const bool match = (shift == 56) || ((key >> (shift + 8)) == (kth >> (shift + 8)));
-            if (match) atomicAdd(&sm.hist[(int)((key >> shift) & 255ull)], 1);
-          }
-          __syncwarp();
-          // bins in descending digit order: lane l holds digits 255-8l .. 248-8l
-          int cl[8], tot = 0;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            cl[e] = sm.hist[255 - 8 * lane - e];
-            tot += cl[e];
-          }
-          const int above_lane = warp_excl_scan(tot, lane);
-          const bool here = above_lane < need && need <= above_lane + tot;
-          const int src = __ffs(__ballot_sync(0xffffffffu, here)) - 1;
-          int digit = 0, above = 0;
-          if (lane == src) {
-            int run = above_lane;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              if (run + cl[e] >= need) {
-                digit = 255 - 8 * lane - e;
-                above = run;
-                break;
-              }
-              run += cl[e];
-            }
-          }
-          digit = __shfl_sync(0xffffffffu, digit, src);
-          above = __shfl_sync(0xffffffffu, above, src);
-          kth |= (unsigned long long)digit << shift;
-          need -= above;
-          __syncwarp();
-        }
-      }
-      float bs = -kInf, bz = 0.f;
-      int bid = INT_MAX;
-      for (int it = 0; it < items.n_it; ++it) {
-        float2 v;
-        if (!items.get(sm.col, sm.dense, it, lane, v)) continue;
-        const int id = __float_as_int(v.y);
-        if (rank_key(v.x, id) >= kth) {
-          const uint32_t x = noise_word((uint32_t)id, t32, rid, ctr3, a.rk0, a.rk1);
-          const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
-          if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
-            bs = scr;
-            bid = id;
-            bz = v.x;
-          }
-        }
-      }
-      const int wl = warp_argmax_lane(bs, bid);
-      w.x = __shfl_sync(0xffffffffu, bz, wl);
-      w.y = __int_as_float(__shfl_sync(0xffffffffu, bid, wl));
+    float2 w;
+    if (items.dense) {
+      w = race_dense(a, sm.dense, ctot, k, tau, t32, rid, ctr3, lane, sm.hist);
+    } else {
+      w = race_generic<NCH>(a, sm, items, ctot, k, tau, t32, rid, ctr3, lane);
     }
 
     // ---- step 5: output

@@ -32,7 +32,7 @@ import torch  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["ds_device.cuh", "ds_sample_common.cuh", "k_sample_warp.cu", "k_sample_cluster.cu",
-                  "k_greedy.cu", "ds_api.cu"]
+                  "k_sample_stream.cu", "k_greedy.cu", "ds_api.cu"]
 
 
 # ------------------------------------------------------------------------------------- helpers

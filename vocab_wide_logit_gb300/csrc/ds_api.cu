@@ -122,8 +122,13 @@ ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void
     const int sms = device_sm_count();
     if (sms <= 0) return DS_ERR_CUDA;
     e = ds::launch_sample_warp(a, st, sms);
+  } else if (4LL * a.k <= (long long)V) {
+    // streaming pass; the cells it cannot finish exactly are marked and
+    // finished by the staged kernel right behind it on the same stream
+    e = ds::launch_sample_stream(a, st);
+    if (e == cudaSuccess) e = ds::launch_sample_cluster(a, st, 1);
   } else {
-    e = ds::launch_sample_cluster(a, st);
+    e = ds::launch_sample_cluster(a, st, 0);
   }
   return e == cudaSuccess ? DS_OK : DS_ERR_CUDA;
 }

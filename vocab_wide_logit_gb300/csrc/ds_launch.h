@@ -8,14 +8,19 @@
 
 namespace ds {
 
-constexpr int kWarpKernelThreads = 128;  // 4 warps per CTA, one cell per warp at a time
+constexpr int kWarpKernelThreads = 128;
+constexpr int kStreamMark = -2;  // out_tokens marker left by the streaming kernel for the staged one  // 4 warps per CTA, one cell per warp at a time
 
 // Largest V of the one-warp-per-cell kernel and of the cluster kernel.
 int warp_kernel_max_vocab();
 int cluster_kernel_max_vocab();
 
 cudaError_t launch_sample_warp(const SampleArgs& a, cudaStream_t st, int num_sms);
-cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st);
+// Staged cluster kernel (z kept in shared memory); with only_marked it finishes
+// just the cells the streaming kernel marked with kStreamMark.
+cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st, int only_marked);
+// Streaming cluster kernel (candidates only in shared memory) for k well below V.
+cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st);
 cudaError_t launch_greedy(const uint16_t* x, int n, int V, float* out_max, float* out_lse, int* out_argmax,
                           cudaStream_t st);
 

@@ -233,7 +233,7 @@ __device__ __forceinline__ float max3c(float a, float b, float c) {
 }
 
 template <int NT, int UNROLL>
-__global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int slice_cap) {
+__global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int slice_cap, int only_marked) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* zs = reinterpret_cast<float*>(smem_raw);
   uint16_t* idxs = reinterpret_cast<uint16_t*>(zs + slice_cap);
@@ -278,6 +278,9 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
   const long long P_u = s_Pu;
 
   for (long long cell = cluster_id; cell < n_cells; cell += n_clusters) {
+    // In fix-up mode only the cells the streaming kernel marked are processed;
+    // every CTA of the cluster reads the same marker before any barrier.
+    if (only_marked && a.out_tokens[cell] != kStreamMark) continue;
     const int c = (int)(cell / P);
     const int p = (int)(cell - (long long)c * P);
     if (wid == 0) {
@@ -656,7 +659,7 @@ constexpr int kSliceCapMax = 16384;
 
 int cluster_kernel_max_vocab() { return 16 * kSliceCapMax - 7; }
 
-cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st) {
+cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st, int only_marked) {
   const int nq_max = (a.V + 7 + 7) >> 3;
   int cs = 1;
   while (cs < 16 && 8 * ((nq_max + cs - 1) / cs) > kSliceCapMax) cs *= 2;
@@ -690,7 +693,7 @@ cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st) {
   long long n_clusters = max_clusters;
   if (n_clusters > n_cells) n_clusters = n_cells;
   cfg.gridDim = dim3((unsigned)(n_clusters * cs), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, a, slice_cap);
+  e = cudaLaunchKernelEx(&cfg, kern, a, slice_cap, only_marked);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -87,7 +87,7 @@ struct CellGeo {
 // get(i), by an 8-bit radix select over a shared-memory histogram (keys are
 // distinct, so exactly one candidate holds it).
 template <typename Get>
-__device__ __noinline__ unsigned long long kth_key(Get get, int n_it, int k, int lane, int* hist) {
+__device__ __forceinline__ unsigned long long kth_key(Get get, int n_it, int k, int lane, int* hist) {
   unsigned long long kth = 0ull;
   int need = k;
   for (int shift = 56; shift >= 0; shift -= 8) {
@@ -135,7 +135,7 @@ __device__ __noinline__ unsigned long long kth_key(Get get, int n_it, int k, int
 
 // Exact race over the candidates at or above key kth: G evaluated exactly for every one.
 template <typename Get>
-__device__ __noinline__ float2 race_exact(const SampleArgs& a, Get get, int n_it, unsigned long long kth, float tau,
+__device__ __forceinline__ float2 race_exact(const SampleArgs& a, Get get, int n_it, unsigned long long kth, float tau,
                                           uint32_t t32, uint32_t rid, uint32_t ctr3) {
   float bs = -kInf, bz = 0.f;
   int bid = INT_MAX;
@@ -159,7 +159,7 @@ __device__ __noinline__ float2 race_exact(const SampleArgs& a, Get get, int n_it
 
 // Exact G for the candidates whose upper bound reaches thr, then the argmax.
 template <typename Get>
-__device__ __noinline__ float2 race_resolve(const SampleArgs& a, Get get, int n_it, float thr, float tau,
+__device__ __forceinline__ float2 race_resolve(const SampleArgs& a, Get get, int n_it, float thr, float tau,
                                             uint32_t t32, uint32_t rid, uint32_t ctr3) {
   float bs = -kInf, bz = 0.f;
   int bid = INT_MAX;
@@ -253,7 +253,7 @@ __device__ __forceinline__ float2 race_dense(const SampleArgs& a, const float2* 
 // The race over per-lane candidate columns (when too many candidates for the
 // balanced list): every step walks the lane's own column.
 template <int NCH>
-__device__ __noinline__ float2 race_generic(const SampleArgs& a, WarpSmem<NCH>& sm, const Items& items, int ctot,
+__device__ __forceinline__ float2 race_generic(const SampleArgs& a, WarpSmem<NCH>& sm, const Items& items, int ctot,
                                             int k, float tau, uint32_t t32, uint32_t rid, uint32_t ctr3, int lane) {
   auto get = [&](int it, float2& v) { return items.get(sm.col, sm.dense, it, lane, v); };
   float loMax = -kInf, hA = -kInf, hB = -kInf;
@@ -319,8 +319,15 @@ __device__ __forceinline__ void load_cell(const CellGeo& G, int lane, uint4 (&rc
   }
 }
 
+#ifndef DS_WARP_MINB
+#define DS_WARP_MINB 4
+#endif
+#ifndef DS_PREFETCH_EARLY
+#define DS_PREFETCH_EARLY 1
+#endif
+
 template <int NCH>
-__global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 6) ? 3 : 2))
+__global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB : ((NCH <= 6) ? 3 : 2))
     k_sample_warp(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   WarpSmem<NCH>& sm = reinterpret_cast<WarpSmem<NCH>*>(smem_raw)[threadIdx.x >> 5];
@@ -568,8 +575,10 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
       cnt = (int)((ca - col0) >> 8);
       ctot = warp_sum_i(cnt);
     }
+#if DS_PREFETCH_EARLY
     // z is dead from here on: start loading the next cell while this one races
     prefetch_next();
+#endif
     const float lse = m + logf(warp_sum(ssum));
     __syncwarp();
     Items items;
@@ -596,6 +605,9 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? 4 : ((NCH <= 
       w = race_generic<NCH>(a, sm, items, ctot, k, tau, t32, rid, ctr3, lane);
     }
 
+#if !DS_PREFETCH_EARLY
+    prefetch_next();
+#endif
     // ---- step 5: output
     if (lane == 0) {
       a.out_tokens[cell] = __float_as_int(w.y);

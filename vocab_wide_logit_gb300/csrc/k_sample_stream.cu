@@ -1,29 +1,29 @@
 // k_sample_stream.cu -- sampling pass for large vocabularies, streaming form:
 // one thread-block cluster per cell, the row split across its CTAs, each logit
-// read once from HBM and never staged.
+// read once from HBM and never staged in full.
 //
 // Per cell, each CTA streams its slice in batches of 16-byte chunks and keeps:
 //   * an online (max, sum of exp(z - max), first argmax) per thread, rescaled
 //     once per batch ("perf: avoid full-vocab all-gather for draft greedy
 //     sampling", LightLLM PR #1517, Design and invariants: per-shard max,
 //     log-sum-exp and argmax, merged with ties to the smallest id);
-//   * the candidates z >= t_b in shared memory, t_b guessed from the moments of
-//     the CTA's first batch.
+//   * in shared memory, only the elements that could still win the Gumbel race
+//     ("Sampler support for discrete diffusion", Hert4's first comment): with
+//     G confined to [G_min, G_max] by the noise map, an element can only win
+//     if z >= max z + tau * (G_min - G_max); the CTA's running max stands in
+//     for max z, which keeps the cut conservative.
 // Then, over distributed shared memory:
-//   R1  max, sum, argmax and max_b t_b   -> lse; the common cut t* = max_b t_b
-//   R2  count(z >= t*) and count(z >= t_hi) over the candidates; the cut must
-//       hold at least k elements (then the kept set -- the k largest z, ties to
-//       the smallest id -- lies inside it)
-//   R3  Gumbel race ("Sampler support for discrete diffusion", Hert4's first
-//       comment): candidates scored with table bounds on G; a candidate whose
-//       best possible score (z + tau * G_max) cannot reach the best lower score
-//       seen so far is skipped without drawing its noise; the cluster keeps the
-//       top two by upper bound
-//   R4  (only if the bounds leave several candidates) exact G for those
-//   R5  (only if the winner lies below t_hi) the winner's rank
-// A cell whose guess fails (too few candidates, a full candidate buffer, or a
-// winner outside the top k) is marked in out_tokens and finished exactly by
-// the staged kernel launched right after this one.
+//   R1  max, sum, argmax, and SA = the best lower-bound score of the candidates
+//       at each CTA's maximum
+//   R3  the race over stored candidates with z >= zmin = SA - tau * G_max (no
+//       other element can reach SA): table bounds on G, cluster top-2 by upper
+//       bound, and C = count(z >= zmin). When C <= k every element above zmin
+//       ranks inside the kept set (the k largest z, ties to the smallest id),
+//       and every kept element below zmin cannot win, so the race is exact
+//       without ever forming the kept set.
+//   R4  (only if the bounds leave several candidates) exact G for those.
+// A cell this cannot settle (C > k, a full candidate buffer) is marked in
+// out_tokens and finished exactly by the staged kernel launched right after.
 #include <cfloat>
 #include <climits>
 #include <cooperative_groups.h>
@@ -67,16 +67,19 @@ __device__ __forceinline__ void msa_merge(float& m, float& s, int& am, float m2,
   m = mm;
 }
 
-// Cluster-wide reduction of a record whose fields combine as: msa triple in
-// (f0, f1, i0), max in f2.., sums in ints i1.. -- the layout of each round is
-// fixed by the caller through the lambdas. Warp 0 combines the CTA's warps and
-// then the cluster's CTAs (lane r reads CTA r's record over DSMEM); every CTA
-// combines the same records in the same order.
+// Float from an order-preserving key (inverse of order_key).
+__device__ __forceinline__ float from_order_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Cluster-wide reduction of one record per CTA: the caller passes a record that
+// is already reduced over its warp (valid in every lane); warp 0 combines the
+// CTA's warps, then the cluster's CTAs (lane r reads CTA r's record over DSMEM).
+// Every CTA combines the same records in the same order.
 template <int NT, typename Comb>
 __device__ __forceinline__ SRec cluster_combine(cg::cluster_group& cl, SXchg& xs, SRec* wrec, const SRec& mine,
                                                 int& parity, int cs, Comb comb) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  // mine is already warp-reduced and valid in lane 0 of every warp
   __syncthreads();
   if (lane == 0) wrec[wid] = mine;
   __syncthreads();
@@ -140,12 +143,14 @@ constexpr int kStreamUnroll = 2;
 
 template <int NT, int UNROLL>
 __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int cap) {
+  constexpr int EPB = 8 * UNROLL;  // elements per thread per batch
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  float2* cand = reinterpret_cast<float2*>(smem_raw);  // [cap] (z, id bits)
+  float2* cand = reinterpret_cast<float2*>(smem_raw);                   // [cap] (z, id bits)
+  float* stage = reinterpret_cast<float*>(cand + cap);                  // [NT][EPB] batch values
   __shared__ SXchg xs;
   __shared__ SRec wrec[NT / 32];
-  __shared__ float wf[NT / 32][4];
   __shared__ int s_ncand;
+  __shared__ uint32_t s_maxkey;
   __shared__ ReqCursor s_cur;
   __shared__ long long s_Pu;
   __shared__ int s_bad;
@@ -160,6 +165,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
   const int P = a.P, V = a.V, k = a.k;
   const float2 neg1 = make_float2(-1.f, -1.f);
   const float2 l2e = make_float2(kLog2e, kLog2e);
+  float* my_stage = stage + tid * EPB;
   int parity = 0;
 
   if (wid == 0) {
@@ -181,8 +187,9 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
     return;  // uniform across the cluster; no shared memory was shared yet
   }
   const long long P_u = s_Pu;
-  // best possible Gumbel value: the upper bound of the last table bucket
+  // range of the noise map: every G lies in [g_min, g_max]
   const float g_max = kGumbelBounds[(1u << (32 - DS_GUMBEL_BUCKET_SHIFT)) - 1].y;
+  const float g_min = kGumbelBounds[0].x;
 
   for (long long cell = cluster_id; cell < n_cells; cell += n_clusters) {
     const int c = (int)(cell / P);
@@ -193,6 +200,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
       if (lane == 0) {
         s_cur = cur;
         s_ncand = 0;
+        s_maxkey = 0u;  // order key below every float
       }
     }
     __syncthreads();
@@ -211,6 +219,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
     const bool guided = g != 0.f;
     const bool sampled = tau > 0.f;
     const float2 g2 = make_float2(g, g);
+    const float reach = tau * (g_max - g_min);  // the most noise can lift one element over another
 
     // ---- slice geometry
     const uint16_t* crow = a.c + cell * (long long)V;
@@ -233,11 +242,8 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
     // ---- streaming pass
     float m = -kInf, s = 0.f;
     int am = INT_MAX;
-    float tb = FLT_MAX;   // this CTA's candidate cut (set after the first batch)
-    float thb = kInf;     // this CTA's upper cut (count(z >= thb) expected below k)
-    float sdb = 0.f;      // this CTA's standard deviation estimate
     bool overflow = false;
-    for (int q0 = q_lo + tid, batch = 0; q0 - tid < q_hi; q0 += NT * UNROLL, ++batch) {
+    for (int q0 = q_lo + tid; q0 - tid < q_hi; q0 += NT * UNROLL) {
       uint4 vc[UNROLL], vu[UNROLL];
 #pragma unroll
       for (int uu = 0; uu < UNROLL; ++uu) {
@@ -295,49 +301,6 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
 #pragma unroll
         for (int i = 0; i < 4; ++i) bm = max3s(bm, z[uu][i].x, z[uu][i].y);
       }
-      if (batch == 0 && sampled) {
-        // candidate cut of this CTA from the moments of its first batch (finite values only)
-        float s1 = 0.f, s2 = 0.f;
-        int n1 = 0;
-#pragma unroll
-        for (int uu = 0; uu < UNROLL; ++uu)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 zz = z[uu][i];
-            const bool fx = zz.x > -kInf, fy = zz.y > -kInf;
-            s1 += (fx ? zz.x : 0.f) + (fy ? zz.y : 0.f);
-            s2 += (fx ? zz.x * zz.x : 0.f) + (fy ? zz.y * zz.y : 0.f);
-            n1 += (int)fx + (int)fy;
-          }
-        s1 = warp_sum(s1);
-        s2 = warp_sum(s2);
-        n1 = warp_sum_i(n1);
-        if (lane == 0) {
-          wf[wid][0] = s1;
-          wf[wid][1] = s2;
-          wf[wid][2] = __int_as_float(n1);
-        }
-        __syncthreads();
-        float S1 = 0.f, S2 = 0.f;
-        int N1 = 0;
-#pragma unroll
-        for (int w = 0; w < NT / 32; ++w) {
-          S1 += wf[w][0];
-          S2 += wf[w][1];
-          N1 += __float_as_int(wf[w][2]);
-        }
-        if (N1 >= 64 && a.q_lo > -kInf) {
-          const float mu = S1 / (float)N1;
-          const float sd = sqrtf(fmaxf(S2 / (float)N1 - mu * mu, 0.f));
-          const float guess = fmaf(sd, a.q_lo, mu);
-          tb = isfinite(guess) ? guess : -FLT_MAX;
-          const float gh = fmaf(sd, a.q_hi, mu);
-          thb = isfinite(gh) ? gh : kInf;
-          sdb = isfinite(sd) ? sd : 0.f;
-        } else {
-          tb = -FLT_MAX;  // keep every finite element
-        }
-      }
       // online max / sum / first argmax (one rescale per batch)
       if (bm > m) {
         s = (m == -kInf) ? 0.f : s * ex2_approx((m - bm) * kLog2e);
@@ -371,34 +334,47 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
         s += (acc0.x + acc0.y) + (acc1.x + acc1.y);
       }
       if (sampled) {
-        // candidates z >= tb: count, reserve a warp range, store
-        int cnt = 0;
+        // keep the elements within `reach` of the CTA's running max
+        const uint32_t old = atomicMax(&s_maxkey, order_key(bm));
+        const float M = fmaxf(from_order_key(old), bm);
+        const float cut = (M > -kInf) ? (M - reach) - (fabsf(M) + reach + 1.f) * 0x1p-16f : kInf;
+        uint32_t mask = 0u;
 #pragma unroll
         for (int uu = 0; uu < UNROLL; ++uu)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) cnt += (z[uu][i].x >= tb) + (z[uu][i].y >= tb);
-        const int ex = warp_excl_scan(cnt, lane);
-        int base = 0;
-        if (lane == 31) base = atomicAdd(&s_ncand, ex + cnt);
-        base = __shfl_sync(0xffffffffu, base, 31);
-        int pos = base + ex;
-        if (pos + cnt > cap) {
-          overflow = true;
-        } else {
+          for (int i = 0; i < 4; ++i) {
+            mask |= (z[uu][i].x >= cut) ? (1u << (8 * uu + 2 * i)) : 0u;
+            mask |= (z[uu][i].y >= cut) ? (1u << (8 * uu + 2 * i + 1)) : 0u;
+          }
+        if (__any_sync(0xffffffffu, mask != 0u)) {
+          const int cnt = __popc(mask);
+          const int ex = warp_excl_scan(cnt, lane);
+          int base = 0;
+          if (lane == 31) base = atomicAdd(&s_ncand, ex + cnt);
+          base = __shfl_sync(0xffffffffu, base, 31);
+          int pos = base + ex;
+          if (pos + cnt > cap) {
+            overflow = true;
+          } else if (mask != 0u) {
+            float4* st4 = reinterpret_cast<float4*>(my_stage);
 #pragma unroll
-          for (int uu = 0; uu < UNROLL; ++uu)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int id = 8 * (q0 + uu * NT) - dc + 2 * i;
-              if (z[uu][i].x >= tb) cand[pos++] = make_float2(z[uu][i].x, __int_as_float(id));
-              if (z[uu][i].y >= tb) cand[pos++] = make_float2(z[uu][i].y, __int_as_float(id + 1));
+            for (int uu = 0; uu < UNROLL; ++uu) {
+              st4[2 * uu] = make_float4(z[uu][0].x, z[uu][0].y, z[uu][1].x, z[uu][1].y);
+              st4[2 * uu + 1] = make_float4(z[uu][2].x, z[uu][2].y, z[uu][3].x, z[uu][3].y);
             }
+            while (mask) {
+              const int b = __ffs(mask) - 1;
+              mask &= mask - 1u;
+              const int id = 8 * (q0 + (b >> 3) * NT) - dc + (b & 7);
+              cand[pos++] = make_float2(my_stage[b], __int_as_float(id));
+            }
+          }
         }
       }
     }
 
-    // ---- R1: max, sum, first argmax, the common cuts, overflow
-    float lse, tstar, thi;
+    // ---- R1: max, sum, first argmax, overflow, and SA from each CTA's top element(s)
+    float lse, SA;
     {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -407,21 +383,34 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
         const int a2 = __shfl_xor_sync(0xffffffffu, am, o);
         msa_merge(m, s, am, m2, s2, a2);
       }
+      __syncthreads();  // s_ncand, s_maxkey and the candidates are final
+      float lo = -kInf;
+      if (sampled) {
+        const float Mb = from_order_key(s_maxkey);
+        const int ncl = min(s_ncand, cap);
+        const uint32_t t32 = (uint32_t)t;
+        const uint32_t ctr3 = a.iter_hi | (uint32_t)c;
+        for (int i = tid; i < ncl; i += NT) {
+          const float2 v = cand[i];
+          if (v.x >= Mb) {  // this CTA's maximum
+            const uint32_t x = noise_word(__float_as_uint(v.y), t32, cur.rid, ctr3, a.rk0, a.rk1);
+            lo = fmaxf(lo, __fmaf_rn(tau, gumbel_bounds(x).x, v.x));
+          }
+        }
+        lo = warp_max(lo);
+      }
       SRec r{};
       r.f[0] = m; r.f[1] = s; r.i[0] = am;
-      r.f[2] = tb;
-      r.f[3] = thb;
+      r.f[2] = lo;
       r.i[1] = __any_sync(0xffffffffu, overflow) ? 1 : 0;
       const SRec R = cluster_combine<NT>(cl, xs, wrec, r, parity, cs, [](SRec& x, const SRec& y) {
         msa_merge(x.f[0], x.f[1], x.i[0], y.f[0], y.f[1], y.i[0]);
         x.f[2] = fmaxf(x.f[2], y.f[2]);
-        x.f[3] = fmaxf(x.f[3], y.f[3]);
         x.i[1] |= y.i[1];
       });
       m = R.f[0];
       lse = (m == -kInf) ? -kInf : m + logf(R.f[1]);
-      tstar = R.f[2];
-      thi = R.f[3];
+      SA = R.f[2];
       if (m == -kInf) {
         if (rank == 0 && tid == 0) {
           a.out_tokens[cell] = 0;
@@ -438,7 +427,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
         __syncthreads();
         continue;
       }
-      if (R.i[1] != 0) {  // some CTA's candidate buffer overflowed: finish in the staged kernel
+      if (R.i[1] != 0 || !(SA > -kInf)) {  // a full candidate buffer: finish in the staged kernel
         if (rank == 0 && tid == 0) a.out_tokens[cell] = kStreamMark;
         __syncthreads();
         continue;
@@ -447,55 +436,20 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
     const int nc = min(s_ncand, cap);
     const uint32_t t32 = (uint32_t)t;
     const uint32_t ctr3 = a.iter_hi | (uint32_t)c;
-
-    // ---- R2: counts at t* and t_hi, and a lower bound SA on the winning score
-    // (the best lower-bound score among the candidates near the maximum)
-    int ctot, chi;
-    float SA;
-    {
-      const float tA = fmaxf(tstar, m - 0.3f * sdb);
-      int c1 = 0, c2 = 0;
-      float lo = -kInf;
-      for (int i = tid; i < nc; i += NT) {
-        const float2 v = cand[i];
-        c1 += (v.x >= tstar) ? 1 : 0;
-        c2 += (v.x >= thi) ? 1 : 0;
-        if (v.x >= tA) {
-          const uint32_t x = noise_word(__float_as_uint(v.y), t32, cur.rid, ctr3, a.rk0, a.rk1);
-          lo = fmaxf(lo, __fmaf_rn(tau, gumbel_bounds(x).x, v.x));
-        }
-      }
-      SRec r{};
-      r.i[0] = warp_sum_i(c1);
-      r.i[1] = warp_sum_i(c2);
-      r.f[0] = warp_max(lo);
-      const SRec R = cluster_combine<NT>(cl, xs, wrec, r, parity, cs, [](SRec& x, const SRec& y) {
-        x.i[0] += y.i[0];
-        x.i[1] += y.i[1];
-        x.f[0] = fmaxf(x.f[0], y.f[0]);
-      });
-      ctot = R.i[0];
-      chi = R.i[1];
-      SA = R.f[0];
-      if (ctot < k) {  // the guess did not cover the top k: finish in the staged kernel
-        if (rank == 0 && tid == 0) a.out_tokens[cell] = kStreamMark;
-        __syncthreads();
-        continue;
-      }
-    }
-
-    // ---- R3: Gumbel race over the candidates that can still win
     const float2 tau2 = make_float2(tau, tau);
+    // nothing below zmin can reach SA, the lower bound of some candidate's score
+    const float zmin = SA - (fabsf(SA) + 1.f) * 0x1p-20f - tau * g_max;
+
+    // ---- R3: the race over the stored candidates >= zmin
     float zw;
     int idw;
     {
-      // a candidate with z + tau * g_max below SA cannot win
-      const float zmin = (SA > -kInf) ? fmaxf(tstar, SA - (fabsf(SA) + 1.f) * 0x1p-20f - tau * g_max) : tstar;
       float loMax = -kInf, hA = -kInf, hB = -kInf;
-      int iA = -1;
+      int iA = -1, cnt = 0;
       for (int i = tid; i < nc; i += NT) {
         const float2 v = cand[i];
         if (v.x >= zmin) {
+          ++cnt;
           const uint32_t x = noise_word(__float_as_uint(v.y), t32, cur.rid, ctr3, a.rk0, a.rk1);
           const float2 sc = __ffma2_rn(tau2, gumbel_bounds(x), make_float2(v.x, v.x));
           loMax = fmaxf(loMax, sc.x);
@@ -511,6 +465,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
         const float hA2 = __shfl_xor_sync(0xffffffffu, hA, o);
         const float hB2 = __shfl_xor_sync(0xffffffffu, hB, o);
         const int iA2 = __shfl_xor_sync(0xffffffffu, iA, o);
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
         loMax = fmaxf(loMax, lm2);
         const bool take = hA2 > hA || (hA2 == hA && iA2 >= 0 && (iA < 0 || iA2 < iA));
         hB = fmaxf(fmaxf(hB, hB2), take ? hA : hA2);
@@ -525,6 +480,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
       r.f[2] = hB;
       r.f[3] = (iA >= 0) ? cand[iA].x : 0.f;
       r.i[0] = (iA >= 0) ? __float_as_int(cand[iA].y) : -1;
+      r.i[1] = cnt;
       const SRec R = cluster_combine<NT>(cl, xs, wrec, r, parity, cs, [](SRec& x, const SRec& y) {
         x.f[0] = fmaxf(x.f[0], y.f[0]);
         const bool take = y.f[1] > x.f[1] || (y.f[1] == x.f[1] && y.i[0] >= 0 && (x.i[0] < 0 || y.i[0] < x.i[0]));
@@ -534,9 +490,11 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
           x.f[3] = y.f[3];
           x.i[0] = y.i[0];
         }
+        x.i[1] += y.i[1];
       });
       const float S = R.f[0];
-      if (!(S > -kInf)) {
+      // every candidate above zmin must rank inside the kept set: count <= k
+      if (!(S > -kInf) || R.i[1] > k) {
         if (rank == 0 && tid == 0) a.out_tokens[cell] = kStreamMark;
         __syncthreads();
         continue;
@@ -574,24 +532,6 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
         idw = R4.i[0];
       }
     }
-    // ---- R5: the winner must rank inside the exact top-k (z desc, id asc), unless
-    // it sits above a cut that holds at most k elements
-    if (ctot > k && !(chi <= k && zw >= thi)) {
-      int rr = 0;
-      for (int i = tid; i < nc; i += NT) {
-        const float2 v = cand[i];
-        rr += (v.x > zw || (v.x == zw && __float_as_int(v.y) < idw)) ? 1 : 0;
-      }
-      SRec r{};
-      r.i[0] = warp_sum_i(rr);
-      const SRec R = cluster_combine<NT>(cl, xs, wrec, r, parity, cs,
-                                         [](SRec& x, const SRec& y) { x.i[0] += y.i[0]; });
-      if (R.i[0] >= k) {
-        if (rank == 0 && tid == 0) a.out_tokens[cell] = kStreamMark;
-        __syncthreads();
-        continue;
-      }
-    }
     if (rank == 0 && tid == 0) {
       a.out_tokens[cell] = idw;
       a.out_logprobs[cell] = zw - lse;
@@ -608,13 +548,13 @@ cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
   int cs = 1;
   while (cs < 8 && nq_max / cs > 2 * kStreamNT * kStreamUnroll) cs *= 2;
   const int slice = 8 * ((nq_max + cs - 1) / cs);
-  // candidate buffer: the expected share of candidates with room to spare
-  const double expect = (double)slice * ((double)a.k / (double)a.V) * 1.05;
-  int cap = (int)(1.4 * expect) + 512;
+  // candidate buffer: a quarter of the slice, at least 2048 entries
+  int cap = slice / 4;
+  if (cap < 2048) cap = 2048;
   if (cap > slice) cap = slice;
-  if (cap > 12288) cap = 12288;
+  if (cap > 8192) cap = 8192;
   auto kern = k_sample_stream<kStreamNT, kStreamUnroll>;
-  const size_t smem = (size_t)cap * sizeof(float2);
+  const size_t smem = (size_t)cap * sizeof(float2) + (size_t)kStreamNT * 8 * kStreamUnroll * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

@@ -5,7 +5,8 @@
 // Per cell, in each CTA:
 //   pass 1  stream the slice in 16-byte chunks: z = c + g (c - u), an online
 //           (max, sum of exp(z - max), first argmax) per thread rescaled once
-//           per batch, and the max of every 8-element chunk into shared memory
+//           per batch, and an upper bound (bf16, rounded up) of every
+//           8-element chunk's max into shared memory
 //   R1      cluster merge of the triples ("perf: avoid full-vocab all-gather for
 //           draft greedy sampling", LightLLM PR #1517, Design and invariants:
 //           per-shard max, log-sum-exp and argmax, ties to the smallest id)
@@ -52,6 +53,14 @@ __device__ __forceinline__ float max3s(float a, float b, float c) {
   return r;
 }
 
+// Smallest bf16 value >= f (f finite or -inf): an upper bound kept in 16 bits.
+__device__ __forceinline__ uint16_t bf16_ceil(float f) {
+  const uint32_t b = __float_as_uint(f);
+  uint32_t hi = b >> 16;
+  if ((b & 0xffffu) != 0u) hi += (b & 0x80000000u) ? 0u : 1u;  // positive: round up; negative: truncation rounds up
+  return (uint16_t)hi;
+}
+
 // Online (max, sum of exp(x - max), first argmax) merge.
 __device__ __forceinline__ void msa_merge(float& m, float& s, int& am, float m2, float s2, int am2) {
   const float mm = fmaxf(m, m2);
@@ -66,11 +75,25 @@ __device__ __forceinline__ void msa_merge(float& m, float& s, int& am, float m2,
   m = mm;
 }
 
-// Cluster-wide reduction of one record per CTA: the caller passes a record that
-// is already reduced over its warp (valid in every lane); warp 0 combines the
-// CTA's warps, then the cluster's CTAs (lane r reads CTA r's record over DSMEM).
-// Every CTA combines the same records in the same order.
-template <int NT, typename Comb>
+// Cluster-wide reduction of one record per CTA. Each warp passes a record already
+// reduced over the warp (valid in every lane); warp 0 combines the CTA's NT/32
+// warp records, then the cluster's CTAs (lane r reads CTA r's record over
+// DSMEM). Only the first NF floats and NI ints are moved. Every CTA combines the
+// same records in the same tree, so every CTA ends with the same result.
+template <int NF, int NI, typename Comb>
+__device__ __forceinline__ void warp_tree(SRec& r, int n, Comb comb) {
+  const int lane = threadIdx.x & 31;
+  for (int o = 1; o < n; o <<= 1) {
+    SRec q;
+#pragma unroll
+    for (int j = 0; j < NF; ++j) q.f[j] = __shfl_down_sync(0xffffffffu, r.f[j], o);
+#pragma unroll
+    for (int j = 0; j < NI; ++j) q.i[j] = __shfl_down_sync(0xffffffffu, r.i[j], o);
+    if ((lane & (2 * o - 1)) == 0 && lane + o < n) comb(r, q);
+  }
+}
+
+template <int NT, int NF, int NI, typename Comb>
 __device__ __forceinline__ SRec cluster_combine(cg::cluster_group& cl, SXchg& xs, SRec* wrec, const SRec& mine,
                                                 int& parity, int cs, Comb comb) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -78,51 +101,14 @@ __device__ __forceinline__ SRec cluster_combine(cg::cluster_group& cl, SXchg& xs
   if (lane == 0) wrec[wid] = mine;
   __syncthreads();
   if (wid == 0) {
-    SRec r = (lane < NT / 32) ? wrec[lane] : SRec{};
-    bool has = lane < NT / 32;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      SRec q;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        q.f[j] = __shfl_xor_sync(0xffffffffu, r.f[j], o);
-        q.i[j] = __shfl_xor_sync(0xffffffffu, r.i[j], o);
-      }
-      const bool qhas = __shfl_xor_sync(0xffffffffu, has, o);
-      if (qhas) {
-        if (has) {
-          // combine in a fixed orientation (lower lane first) for determinism
-          if ((lane & o) == 0) comb(r, q); else { comb(q, r); r = q; }
-        } else {
-          r = q;
-        }
-        has = true;
-      }
-    }
+    SRec r = wrec[lane < NT / 32 ? lane : 0];
+    warp_tree<NF, NI>(r, NT / 32, comb);
     if (lane == 0) xs.slot[parity] = r;
   }
   cl.sync();
   if (wid == 0) {
     SRec r = *cl.map_shared_rank(&xs.slot[parity], lane < cs ? lane : 0);
-    bool has = lane < cs;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      SRec q;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        q.f[j] = __shfl_xor_sync(0xffffffffu, r.f[j], o);
-        q.i[j] = __shfl_xor_sync(0xffffffffu, r.i[j], o);
-      }
-      const bool qhas = __shfl_xor_sync(0xffffffffu, has, o);
-      if (qhas) {
-        if (has) {
-          if ((lane & o) == 0) comb(r, q); else { comb(q, r); r = q; }
-        } else {
-          r = q;
-        }
-        has = true;
-      }
-    }
+    warp_tree<NF, NI>(r, cs, comb);
     if (lane == 0) xs.comb = r;
   }
   __syncthreads();
@@ -139,8 +125,8 @@ template <int NT, int UNROLL>
 __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int chunk_cap, int cap) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float2* cand = reinterpret_cast<float2*>(smem_raw);           // [cap] (z, id bits)
-  float* cmax = reinterpret_cast<float*>(cand + cap);           // [chunk_cap] per-chunk maxima
-  uint16_t* hot = reinterpret_cast<uint16_t*>(cmax + chunk_cap);  // [chunk_cap] chunks to revisit
+  uint16_t* cmax = reinterpret_cast<uint16_t*>(cand + cap);     // [chunk_cap] chunk maxima, bf16 rounded up
+  uint16_t* hot = cmax + chunk_cap;                             // [chunk_cap] chunks to revisit
   __shared__ SXchg xs;
   __shared__ SRec wrec[NT / 32];
   __shared__ int s_nhot, s_ncand;
@@ -288,7 +274,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
         cm = max3s(cm, z[uu][2].y, z[uu][3].x);
         cm = fmaxf(cm, z[uu][3].y);
         if (q >= q_hi) cm = -kInf;
-        else cmax[q - q_lo] = cm;
+        else cmax[q - q_lo] = bf16_ceil(cm);
         bm = fmaxf(bm, cm);
       }
       if (bm > m) {  // new running max: rescale the sum, take the first id attaining it
@@ -336,7 +322,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
       }
       SRec r{};
       r.f[0] = m; r.f[1] = s; r.i[0] = am;
-      const SRec R = cluster_combine<NT>(cl, xs, wrec, r, parity, cs, [](SRec& x, const SRec& y) {
+      const SRec R = cluster_combine<NT, 2, 1>(cl, xs, wrec, r, parity, cs, [](SRec& x, const SRec& y) {
         msa_merge(x.f[0], x.f[1], x.i[0], y.f[0], y.f[1], y.i[0]);
       });
       m = R.f[0];
@@ -361,7 +347,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
     const int n_loc = q_hi - q_lo;
     for (int j0 = 0; j0 < n_loc; j0 += NT) {
       const int j = j0 + tid;
-      const bool h = (j < n_loc) && (cmax[j] >= zmin);
+      const bool h = (j < n_loc) && (__uint_as_float((uint32_t)cmax[j] << 16) >= zmin);
       const unsigned b = __ballot_sync(0xffffffffu, h);
       if (b) {
         int base = 0;
@@ -431,9 +417,9 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
       r.f[2] = hB;
       r.f[3] = (iA >= 0) ? cand[iA].x : 0.f;
       r.i[0] = (iA >= 0) ? __float_as_int(cand[iA].y) : -1;
-      r.i[1] = nc_all;
+      r.i[1] = (wid == 0) ? nc_all : 0;  // a CTA-wide value: count it once per CTA
       r.i[2] = (nc_all > cap) ? 1 : 0;
-      const SRec R = cluster_combine<NT>(cl, xs, wrec, r, parity, cs, [](SRec& x, const SRec& y) {
+      const SRec R = cluster_combine<NT, 4, 3>(cl, xs, wrec, r, parity, cs, [](SRec& x, const SRec& y) {
         x.f[0] = fmaxf(x.f[0], y.f[0]);
         const bool take = y.f[1] > x.f[1] || (y.f[1] == x.f[1] && y.i[0] >= 0 && (x.i[0] < 0 || y.i[0] < x.i[0]));
         x.f[2] = fmaxf(fmaxf(x.f[2], y.f[2]), take ? x.f[1] : y.f[1]);
@@ -476,7 +462,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
         r4.f[0] = __shfl_sync(0xffffffffu, bs, wl);
         r4.f[1] = __shfl_sync(0xffffffffu, bz, wl);
         r4.i[0] = __shfl_sync(0xffffffffu, bid, wl);
-        const SRec R4 = cluster_combine<NT>(cl, xs, wrec, r4, parity, cs, [](SRec& x, const SRec& y) {
+        const SRec R4 = cluster_combine<NT, 2, 1>(cl, xs, wrec, r4, parity, cs, [](SRec& x, const SRec& y) {
           if (y.f[0] > x.f[0] || (y.f[0] == x.f[0] && y.i[0] < x.i[0])) x = y;
         });
         zw = R4.f[1];
@@ -495,14 +481,14 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
 // ---------------------------------------------------------------- launcher
 cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
   const int nq_max = (a.V + 7 + 7) >> 3;
-  // 8 CTAs per row for the large vocabularies, fewer for shorter rows
+  // up to 4 CTAs per row: enough logits per thread to amortise the per-cell rounds
   int cs = 1;
-  while (cs < 8 && nq_max / cs > 2 * kStreamNT * kStreamUnroll) cs *= 2;
+  while (cs < 4 && nq_max / cs > 2 * kStreamNT * kStreamUnroll) cs *= 2;
   const int chunk_cap = (nq_max + cs - 1) / cs + 1;
   if (chunk_cap > 65535) return cudaErrorInvalidValue;
-  const int cap = 4096;
+  const int cap = 2048;
   auto kern = k_sample_stream<kStreamNT, kStreamUnroll>;
-  const size_t smem = (size_t)cap * sizeof(float2) + (size_t)chunk_cap * (sizeof(float) + sizeof(uint16_t)) + 16;
+  const size_t smem = (size_t)cap * sizeof(float2) + (size_t)chunk_cap * 2 * sizeof(uint16_t) + 16;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

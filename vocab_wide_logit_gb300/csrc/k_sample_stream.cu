@@ -27,6 +27,7 @@
 #include <cfloat>
 #include <climits>
 #include <cooperative_groups.h>
+#include <type_traits>
 
 #include "ds_launch.h"
 #include "ds_sample_common.cuh"
@@ -252,63 +253,108 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
       return make_uint4(w[0], w[1], w[2], w[3]);
     };
 
-    // ---- pass 1: stream the slice once
+    // ---- pass 1: stream the slice once. Interior chunks go through full
+    // batches with no per-chunk checks; the row's edge chunks and the last
+    // partial batch go through a checked one-chunk path.
     float m = -kInf, s = 0.f;
     int am = INT_MAX;
-    for (int q0 = q_lo + tid; q0 - tid < q_hi; q0 += NT * UNROLL) {
-      uint4 vc[UNROLL], vu[UNROLL];
+    auto pass1 = [&](auto guided_tag) {
+      constexpr bool GD = decltype(guided_tag)::value;
+      // one batch of NCHK chunks at q0, q0 + NT, ...; CHECKED: mask edges and skip q >= q_hi
+      auto batch = [&](int q0, auto nchk_tag, auto checked_tag) {
+        constexpr int NCHK = decltype(nchk_tag)::value;
+        constexpr bool CHECKED = decltype(checked_tag)::value;
+        uint4 vc[NCHK], vu[NCHK];
 #pragma unroll
-      for (int uu = 0; uu < UNROLL; ++uu) {
-        const int q = q0 + uu * NT;
-        vc[uu] = (q < q_hi) ? ld_stream16(cb + q) : make_uint4(0u, 0u, 0u, 0u);
-        vu[uu] = (q < q_hi) ? load_u(q) : make_uint4(0u, 0u, 0u, 0u);
-      }
-      float2 z[UNROLL][4];
-      float bm = -kInf;
-#pragma unroll
-      for (int uu = 0; uu < UNROLL; ++uu) {
-        const int q = q0 + uu * NT;
-        chunk_z(q, vc[uu], vu[uu], z[uu]);
-        float cm = max3s(z[uu][0].x, z[uu][0].y, z[uu][1].x);
-        cm = max3s(cm, z[uu][1].y, z[uu][2].x);
-        cm = max3s(cm, z[uu][2].y, z[uu][3].x);
-        cm = fmaxf(cm, z[uu][3].y);
-        if (q >= q_hi) cm = -kInf;
-        else cmax[q - q_lo] = bf16_ceil(cm);
-        bm = fmaxf(bm, cm);
-      }
-      if (bm > m) {  // new running max: rescale the sum, take the first id attaining it
-        s = (m == -kInf) ? 0.f : s * ex2_approx((m - bm) * kLog2e);
-        m = bm;
-        int aa = INT_MAX;
-#pragma unroll
-        for (int uu = UNROLL - 1; uu >= 0; --uu) {
-          if (q0 + uu * NT >= q_hi) continue;  // beyond the slice
-#pragma unroll
-          for (int i = 3; i >= 0; --i) {
-            const int id = 8 * (q0 + uu * NT) - dc + 2 * i;
-            if (z[uu][i].y == bm) aa = id + 1;
-            if (z[uu][i].x == bm) aa = id;
-          }
+        for (int uu = 0; uu < NCHK; ++uu) {
+          const int q = q0 + uu * NT;
+          const bool ok = !CHECKED || q < q_hi;
+          vc[uu] = ok ? ld_stream16(cb + q) : make_uint4(0u, 0u, 0u, 0u);
+          if (GD) vu[uu] = ok ? load_u(q) : make_uint4(0u, 0u, 0u, 0u);
         }
-        am = aa;
-      }
-      if (m != -kInf) {
-        const float2 nml = make_float2(-m * kLog2e, -m * kLog2e);
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        float2 z[NCHK][4];
+        float bm = -kInf;
 #pragma unroll
-        for (int uu = 0; uu < UNROLL; ++uu) {
-          const bool in = q0 + uu * NT < q_hi;
+        for (int uu = 0; uu < NCHK; ++uu) {
+          const int q = q0 + uu * NT;
+          const uint32_t wc[4] = {vc[uu].x, vc[uu].y, vc[uu].z, vc[uu].w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float2 tt = __ffma2_rn(z[uu][i], l2e, nml);
-            const float2 ee = make_float2(in ? ex2_approx(tt.x) : 0.f, in ? ex2_approx(tt.y) : 0.f);
-            if (i & 1) acc1 = __fadd2_rn(acc1, ee); else acc0 = __fadd2_rn(acc0, ee);
+            const float2 cp = make_float2(bf_lo(wc[i]), bf_hi(wc[i]));
+            if (GD) {
+              const uint32_t wu = (i == 0) ? vu[uu].x : (i == 1) ? vu[uu].y : (i == 2) ? vu[uu].z : vu[uu].w;
+              const float2 up = make_float2(bf_lo(wu), bf_hi(wu));
+              z[uu][i] = __ffma2_rn(g2, __ffma2_rn(up, neg1, cp), cp);  // fl(c - u), then one fma
+            } else {
+              z[uu][i] = cp;
+            }
           }
+          if (CHECKED) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int id = 8 * q - dc + 2 * i;
+              if (q >= q_hi || id < 0 || id >= V) z[uu][i].x = -kInf;
+              if (q >= q_hi || id + 1 < 0 || id + 1 >= V) z[uu][i].y = -kInf;
+            }
+          }
+          float cm = max3s(z[uu][0].x, z[uu][0].y, z[uu][1].x);
+          cm = max3s(cm, z[uu][1].y, z[uu][2].x);
+          cm = max3s(cm, z[uu][2].y, z[uu][3].x);
+          cm = fmaxf(cm, z[uu][3].y);
+          if (!CHECKED || q < q_hi) cmax[q - q_lo] = bf16_ceil(cm);
+          bm = fmaxf(bm, cm);
         }
-        s += (acc0.x + acc0.y) + (acc1.x + acc1.y);
-      }
-    }
+        if (bm >= m && bm > -kInf) {
+          // a new (or equal) running max: rescale the sum; keep the smallest id
+          // attaining it (chunks are not visited in id order, so take the min)
+          if (bm > m) {
+            s = (m == -kInf) ? 0.f : s * ex2_approx((m - bm) * kLog2e);
+            m = bm;
+            am = INT_MAX;
+          }
+          int aa = INT_MAX;
+#pragma unroll
+          for (int uu = NCHK - 1; uu >= 0; --uu) {
+#pragma unroll
+            for (int i = 3; i >= 0; --i) {
+              const int id = 8 * (q0 + uu * NT) - dc + 2 * i;
+              if (z[uu][i].y == bm) aa = id + 1;
+              if (z[uu][i].x == bm) aa = id;
+            }
+          }
+          am = min(am, aa);
+        }
+        if (m != -kInf) {
+          const float2 nml = make_float2(-m * kLog2e, -m * kLog2e);
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int uu = 0; uu < NCHK; ++uu)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 tt = __ffma2_rn(z[uu][i], l2e, nml);
+              const float2 ee = make_float2(ex2_approx(tt.x), ex2_approx(tt.y));
+              if (i & 1) acc1 = __fadd2_rn(acc1, ee); else acc0 = __fadd2_rn(acc0, ee);
+            }
+          s += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+        }
+      };
+      // interior chunks [qa, qb): no row edges inside
+      if (tid == 0 && q_lo == 0 && q_hi > 0) batch(0, std::integral_constant<int, 1>{}, std::true_type{});
+      const int qa = max(q_lo, 1), qb = min(q_hi, nq - 1);
+      const int n_full = (qb > qa) ? (qb - qa) / (NT * UNROLL) : 0;
+      int q0 = qa + tid;
+      for (int b = 0; b < n_full; ++b, q0 += NT * UNROLL)
+        batch(q0, std::integral_constant<int, UNROLL>{}, std::false_type{});
+      // the rest of [qa, qb), then the row-edge chunks of this slice, one at a time
+      for (int q = qa + n_full * NT * UNROLL + tid; q < qb; q += NT)
+        batch(q, std::integral_constant<int, 1>{}, std::true_type{});
+      if (tid == 0 && nq - 1 >= max(q_lo, 1) && nq - 1 < q_hi)
+        batch(nq - 1, std::integral_constant<int, 1>{}, std::true_type{});
+    };
+    if (guided)
+      pass1(std::true_type{});
+    else
+      pass1(std::false_type{});
 
     // ---- R1: cluster max, sum and first argmax
     float lse;
@@ -486,7 +532,7 @@ cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
   while (cs < 4 && nq_max / cs > 2 * kStreamNT * kStreamUnroll) cs *= 2;
   const int chunk_cap = (nq_max + cs - 1) / cs + 1;
   if (chunk_cap > 65535) return cudaErrorInvalidValue;
-  const int cap = 2048;
+  const int cap = 4096;
   auto kern = k_sample_stream<kStreamNT, kStreamUnroll>;
   const size_t smem = (size_t)cap * sizeof(float2) + (size_t)chunk_cap * 2 * sizeof(uint16_t) + 16;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -7,11 +7,13 @@
 // cluster that splits a row, and the merge runs over distributed shared
 // memory instead of an all-gather between GPUs.
 //
-// One streaming pass: each thread walks 16-byte chunks in increasing id order
-// keeping an online (max, sum of exp(x - max), first argmax); a chunk's eight
-// values are folded with one rescale per chunk, so each logit costs one exp.
+// One streaming pass: each thread walks 16-byte chunks keeping an online (max,
+// sum of exp(x - max), smallest argmax), rescaled once per batch of chunks, so
+// each logit costs one exp. Interior chunks run in unchecked batches; only the
+// row's first and last chunk go through the masked path.
 #include <climits>
 #include <cooperative_groups.h>
+#include <type_traits>
 
 #include "ds_device.cuh"
 #include "ds_launch.h"
@@ -79,22 +81,26 @@ __global__ void __launch_bounds__(NT) k_greedy_lse(const uint16_t* __restrict__ 
     const int q_hi = (int)((long long)(rank + 1) * nq / cs);
 
     Triple t{-kInf, 0.f, INT_MAX};
-    for (int q0 = q_lo + tid; q0 < q_hi; q0 += NT * UNROLL) {
-      uint4 v[UNROLL];
+    // one batch of NCHK chunks at q0, q0 + NT, ...; CHECKED masks the row edges
+    // and skips chunks beyond the slice
+    auto batch = [&](int q0, auto nchk_tag, auto checked_tag) {
+      constexpr int NCHK = decltype(nchk_tag)::value;
+      constexpr bool CHECKED = decltype(checked_tag)::value;
+      uint4 v[NCHK];
 #pragma unroll
-      for (int u = 0; u < UNROLL; ++u) {
+      for (int u = 0; u < NCHK; ++u) {
         const int q = q0 + u * NT;
-        v[u] = (q < q_hi) ? ld_stream16(base + q) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+        v[u] = (!CHECKED || q < q_hi) ? ld_stream16(base + q) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
       }
-      float2 f[UNROLL][4];
+      float2 f[NCHK][4];
       float bm = -kInf;
 #pragma unroll
-      for (int u = 0; u < UNROLL; ++u) {
+      for (int u = 0; u < NCHK; ++u) {
         const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) f[u][i] = make_float2(bf_lo(w[i]), bf_hi(w[i]));
-        const int q = q0 + u * NT;
-        if (q == 0 || q >= nq - 1) {  // row edges: mask the ids outside [0, V)
+        if (CHECKED) {
+          const int q = q0 + u * NT;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int id = 8 * q - dc + 2 * i;
@@ -105,34 +111,49 @@ __global__ void __launch_bounds__(NT) k_greedy_lse(const uint16_t* __restrict__ 
 #pragma unroll
         for (int i = 0; i < 4; ++i) bm = max3g(bm, f[u][i].x, f[u][i].y);
       }
-      if (bm > t.m) {
-        // new running max: rescale the sum and take the first id attaining it
-        t.s = (t.m == -kInf) ? 0.f : t.s * ex2_approx((t.m - bm) * kLog2e);
-        t.m = bm;
+      if (bm >= t.m && bm > -kInf) {
+        // new (or equal) running max: rescale the sum; keep the smallest id attaining it
+        if (bm > t.m) {
+          t.s = (t.m == -kInf) ? 0.f : t.s * ex2_approx((t.m - bm) * kLog2e);
+          t.m = bm;
+          t.a = INT_MAX;
+        }
         int a = INT_MAX;
 #pragma unroll
-        for (int u = UNROLL - 1; u >= 0; --u)
+        for (int u = NCHK - 1; u >= 0; --u)
 #pragma unroll
           for (int i = 3; i >= 0; --i) {
             const int id = 8 * (q0 + u * NT) - dc + 2 * i;
             if (f[u][i].y == bm) a = id + 1;
             if (f[u][i].x == bm) a = id;
           }
-        t.a = a;
+        t.a = min(t.a, a);
       }
       if (t.m != -kInf) {
         const float2 nml = make_float2(-t.m * kLog2e, -t.m * kLog2e);
-        float2 acc = make_float2(0.f, 0.f);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u)
+        for (int u = 0; u < NCHK; ++u)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 tt = __ffma2_rn(f[u][i], l2e, nml);
-            acc = __fadd2_rn(acc, make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
+            const float2 ee = make_float2(ex2_approx(tt.x), ex2_approx(tt.y));
+            if (i & 1) acc1 = __fadd2_rn(acc1, ee); else acc0 = __fadd2_rn(acc0, ee);
           }
-        t.s += acc.x + acc.y;
+        t.s += (acc0.x + acc0.y) + (acc1.x + acc1.y);
       }
-    }
+    };
+    // row-edge chunk 0, full batches of interior chunks, the remainder, then chunk nq-1
+    if (tid == 0 && q_lo == 0 && q_hi > 0) batch(0, std::integral_constant<int, 1>{}, std::true_type{});
+    const int qa = max(q_lo, 1), qb = min(q_hi, nq - 1);
+    const int n_full = (qb > qa) ? (qb - qa) / (NT * UNROLL) : 0;
+    int q0 = qa + tid;
+    for (int b = 0; b < n_full; ++b, q0 += NT * UNROLL)
+      batch(q0, std::integral_constant<int, UNROLL>{}, std::false_type{});
+    for (int q = qa + n_full * NT * UNROLL + tid; q < qb; q += NT)
+      batch(q, std::integral_constant<int, 1>{}, std::false_type{});
+    if (tid == 0 && nq - 1 >= max(q_lo, 1) && nq - 1 < q_hi)
+      batch(nq - 1, std::integral_constant<int, 1>{}, std::true_type{});
     // block merge
     t = warp_merge(t);
     if (lane == 0) warp_part[wid] = t;

@@ -319,8 +319,11 @@ __device__ __forceinline__ void load_cell(const CellGeo& G, int lane, uint4 (&rc
   }
 }
 
+// Occupancy and prefetch placement (measured on GB300 at V = 1025): 3 CTAs of 4
+// warps per SM with the next cell's loads issued before the race is fastest;
+// a 4-CTA register budget spills.
 #ifndef DS_WARP_MINB
-#define DS_WARP_MINB 4
+#define DS_WARP_MINB 3
 #endif
 #ifndef DS_PREFETCH_EARLY
 #define DS_PREFETCH_EARLY 1

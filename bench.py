@@ -339,7 +339,7 @@ def run_ours(args):
                 torch.cuda.empty_cache()
                 ow = make_workload(other)
                 runner = GreedyRunner(ow, dev) if other == "cfg4" else SampleRunner(ow, dev)
-                oms = time_steps(runner, max(10, args.steps), args.warmup, 1)
+                oms = time_steps(runner, max(10, min(args.steps, 1500)), args.warmup, 1)
                 extra[other] = {"workload": ow.name, "ms_per_step": round(oms, 5),
                                 "units_per_s": round(runner.units / (oms / 1e3), 1),
                                 "roofline": roofline(runner.bytes_per_step, oms, other)}
@@ -387,8 +387,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["cfg3", "cfg5", "cfg4", "cfg1", "cfg2"], default="cfg3")
     ap.add_argument("--no-extra", action="store_true", help="skip the large-vocab lines under 'also'")

@@ -60,7 +60,7 @@ __device__ __forceinline__ float max3g(float a, float b, float c) {
 }
 
 template <int NT, int UNROLL>
-__global__ void __launch_bounds__(NT) k_greedy_lse(const uint16_t* __restrict__ x, int n, int V,
+__global__ void __launch_bounds__(NT, 4) k_greedy_lse(const uint16_t* __restrict__ x, int n, int V,
                                                   float* __restrict__ out_max, float* __restrict__ out_lse,
                                                   int* __restrict__ out_argmax) {
   __shared__ Triple warp_part[NT / 32];
@@ -83,15 +83,18 @@ __global__ void __launch_bounds__(NT) k_greedy_lse(const uint16_t* __restrict__ 
     Triple t{-kInf, 0.f, INT_MAX};
     // one batch of NCHK chunks at q0, q0 + NT, ...; CHECKED masks the row edges
     // and skips chunks beyond the slice
-    auto batch = [&](int q0, auto nchk_tag, auto checked_tag) {
+    auto load = [&](int q0, auto nchk_tag, auto checked_tag, uint4* v) {
       constexpr int NCHK = decltype(nchk_tag)::value;
       constexpr bool CHECKED = decltype(checked_tag)::value;
-      uint4 v[NCHK];
 #pragma unroll
       for (int u = 0; u < NCHK; ++u) {
         const int q = q0 + u * NT;
         v[u] = (!CHECKED || q < q_hi) ? ld_stream16(base + q) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
       }
+    };
+    auto compute = [&](int q0, auto nchk_tag, auto checked_tag, const uint4* v) {
+      constexpr int NCHK = decltype(nchk_tag)::value;
+      constexpr bool CHECKED = decltype(checked_tag)::value;
       float2 f[NCHK][4];
       float bm = -kInf;
 #pragma unroll
@@ -143,17 +146,31 @@ __global__ void __launch_bounds__(NT) k_greedy_lse(const uint16_t* __restrict__ 
         t.s += (acc0.x + acc0.y) + (acc1.x + acc1.y);
       }
     };
-    // row-edge chunk 0, full batches of interior chunks, the remainder, then chunk nq-1
-    if (tid == 0 && q_lo == 0 && q_hi > 0) batch(0, std::integral_constant<int, 1>{}, std::true_type{});
+    auto batch = [&](int q0, auto nchk_tag, auto checked_tag) {
+      uint4 v[decltype(nchk_tag)::value];
+      load(q0, nchk_tag, checked_tag, v);
+      compute(q0, nchk_tag, checked_tag, v);
+    };
+    using UN = std::integral_constant<int, UNROLL>;
+    using ONE = std::integral_constant<int, 1>;
+    // row-edge chunk 0, full batches of interior chunks (the next batch's loads
+    // in flight while this one is reduced), the remainder, then chunk nq-1
+    if (tid == 0 && q_lo == 0 && q_hi > 0) batch(0, ONE{}, std::true_type{});
     const int qa = max(q_lo, 1), qb = min(q_hi, nq - 1);
     const int n_full = (qb > qa) ? (qb - qa) / (NT * UNROLL) : 0;
     int q0 = qa + tid;
-    for (int b = 0; b < n_full; ++b, q0 += NT * UNROLL)
-      batch(q0, std::integral_constant<int, UNROLL>{}, std::false_type{});
-    for (int q = qa + n_full * NT * UNROLL + tid; q < qb; q += NT)
-      batch(q, std::integral_constant<int, 1>{}, std::false_type{});
-    if (tid == 0 && nq - 1 >= max(q_lo, 1) && nq - 1 < q_hi)
-      batch(nq - 1, std::integral_constant<int, 1>{}, std::true_type{});
+    if (n_full > 0) {
+      uint4 cur[UNROLL], nxt[UNROLL];
+      load(q0, UN{}, std::false_type{}, cur);
+      for (int b = 0; b < n_full; ++b, q0 += NT * UNROLL) {
+        if (b + 1 < n_full) load(q0 + NT * UNROLL, UN{}, std::false_type{}, nxt);
+        compute(q0, UN{}, std::false_type{}, cur);
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) cur[u] = nxt[u];
+      }
+    }
+    for (int q = qa + n_full * NT * UNROLL + tid; q < qb; q += NT) batch(q, ONE{}, std::false_type{});
+    if (tid == 0 && nq - 1 >= max(q_lo, 1) && nq - 1 < q_hi) batch(nq - 1, ONE{}, std::true_type{});
     // block merge
     t = warp_merge(t);
     if (lane == 0) warp_part[wid] = t;

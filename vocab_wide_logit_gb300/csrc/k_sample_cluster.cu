@@ -691,6 +691,8 @@ cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st, int only
   if (max_clusters < 1) return cudaErrorLaunchOutOfResources;
   const long long n_cells = (long long)a.C * a.P;
   long long n_clusters = max_clusters;
+  // in fix-up mode the marked cells are rare: a few clusters scan the markers
+  if (only_marked && n_clusters > 4) n_clusters = 4;
   if (n_clusters > n_cells) n_clusters = n_cells;
   cfg.gridDim = dim3((unsigned)(n_clusters * cs), 1, 1);
   e = cudaLaunchKernelEx(&cfg, kern, a, slice_cap, only_marked);

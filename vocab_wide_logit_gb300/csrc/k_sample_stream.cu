@@ -261,10 +261,9 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
     auto pass1 = [&](auto guided_tag) {
       constexpr bool GD = decltype(guided_tag)::value;
       // one batch of NCHK chunks at q0, q0 + NT, ...; CHECKED: mask edges and skip q >= q_hi
-      auto batch = [&](int q0, auto nchk_tag, auto checked_tag) {
+      auto load = [&](int q0, auto nchk_tag, auto checked_tag, uint4* vc, uint4* vu) {
         constexpr int NCHK = decltype(nchk_tag)::value;
         constexpr bool CHECKED = decltype(checked_tag)::value;
-        uint4 vc[NCHK], vu[NCHK];
 #pragma unroll
         for (int uu = 0; uu < NCHK; ++uu) {
           const int q = q0 + uu * NT;
@@ -272,6 +271,10 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
           vc[uu] = ok ? ld_stream16(cb + q) : make_uint4(0u, 0u, 0u, 0u);
           if (GD) vu[uu] = ok ? load_u(q) : make_uint4(0u, 0u, 0u, 0u);
         }
+      };
+      auto compute = [&](int q0, auto nchk_tag, auto checked_tag, const uint4* vc, const uint4* vu) {
+        constexpr int NCHK = decltype(nchk_tag)::value;
+        constexpr bool CHECKED = decltype(checked_tag)::value;
         float2 z[NCHK][4];
         float bm = -kInf;
 #pragma unroll
@@ -339,17 +342,34 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int
         }
       };
       // interior chunks [qa, qb): no row edges inside
-      if (tid == 0 && q_lo == 0 && q_hi > 0) batch(0, std::integral_constant<int, 1>{}, std::true_type{});
+      auto batch = [&](int q0, auto nchk_tag, auto checked_tag) {
+        uint4 vc[decltype(nchk_tag)::value], vu[decltype(nchk_tag)::value];
+        load(q0, nchk_tag, checked_tag, vc, vu);
+        compute(q0, nchk_tag, checked_tag, vc, vu);
+      };
+      using UN = std::integral_constant<int, UNROLL>;
+      using ONE = std::integral_constant<int, 1>;
+      if (tid == 0 && q_lo == 0 && q_hi > 0) batch(0, ONE{}, std::true_type{});
       const int qa = max(q_lo, 1), qb = min(q_hi, nq - 1);
       const int n_full = (qb > qa) ? (qb - qa) / (NT * UNROLL) : 0;
       int q0 = qa + tid;
-      for (int b = 0; b < n_full; ++b, q0 += NT * UNROLL)
-        batch(q0, std::integral_constant<int, UNROLL>{}, std::false_type{});
-      // the rest of [qa, qb), then the row-edge chunks of this slice, one at a time
-      for (int q = qa + n_full * NT * UNROLL + tid; q < qb; q += NT)
-        batch(q, std::integral_constant<int, 1>{}, std::true_type{});
-      if (tid == 0 && nq - 1 >= max(q_lo, 1) && nq - 1 < q_hi)
-        batch(nq - 1, std::integral_constant<int, 1>{}, std::true_type{});
+      if (n_full > 0) {
+        // the next batch's loads are in flight while this one is reduced
+        uint4 cc[UNROLL], cu[UNROLL], nc_[UNROLL], nu[UNROLL];
+        load(q0, UN{}, std::false_type{}, cc, cu);
+        for (int b = 0; b < n_full; ++b, q0 += NT * UNROLL) {
+          if (b + 1 < n_full) load(q0 + NT * UNROLL, UN{}, std::false_type{}, nc_, nu);
+          compute(q0, UN{}, std::false_type{}, cc, cu);
+#pragma unroll
+          for (int uu = 0; uu < UNROLL; ++uu) {
+            cc[uu] = nc_[uu];
+            cu[uu] = nu[uu];
+          }
+        }
+      }
+      // the rest of [qa, qb), then the row-edge chunk nq-1, one chunk at a time
+      for (int q = qa + n_full * NT * UNROLL + tid; q < qb; q += NT) batch(q, ONE{}, std::true_type{});
+      if (tid == 0 && nq - 1 >= max(q_lo, 1) && nq - 1 < q_hi) batch(nq - 1, ONE{}, std::true_type{});
     };
     if (guided)
       pass1(std::true_type{});

@@ -200,7 +200,7 @@ def test_unguided_batch_passes_no_u():
         assert int(d.status.item()) == 0
 
 
-def _planted(V, C, T, tie_at, k_ratio, seed):
+def _planted(V, C, T, seed):
     """Rows where the logits hold many exact ties: at the maximum, and straddling the top-k cut."""
     rng = np.random.Generator(np.random.PCG64(seed))
     base = np.round(rng.standard_normal((C, T, V)) * 2.0 * 4) / 4  # quarter steps: plenty of equal values
@@ -213,7 +213,7 @@ def test_exact_ties_at_max_and_at_cut(V):
     kept set must take the smallest ids; the max is tied too (smallest id for temperature 0)."""
     dev = _dev()
     C, T = 1, 6
-    z = _planted(V, C, T, None, 0.1, 21)
+    z = _planted(V, C, T, 21)
     c = wl.to_bf16(z)
     inp = wl.SampleInputs(name="ties", C=C, V=V, seq_lens=np.array([T], np.int32),
                           request_ids=np.array([77], np.int32), guidance=np.array([0.0], np.float32),
@@ -327,3 +327,17 @@ def test_empty_calls_launch_nothing():
     assert pkg.ds_sample(e, c, None, e, f, f, 0.1, 0, 0, e, f, B=0, C=2, P=0, V=1025) == 0
     x = torch.empty((0, 100), dtype=torch.bfloat16, device=dev)
     assert pkg.ds_greedy_lse(x, f, f, e) == 0
+
+
+def test_large_vocab_hot_temperatures_take_the_exact_path():
+    """High temperatures widen the set of tokens that can still win the race; cells the
+    streaming pass cannot settle are finished by the staged pass in the same call. Mixed
+    temperatures in one batch exercise both in one launch pair."""
+    dev = _dev()
+    inp = wl.make_sample_inputs("hot", C=1, seq_lens=[3, 3, 2], V=131072, guidance=[1.0, 0.0, 2.0],
+                                temperature=[4.0, 0.7, 9.0], sigma_c=1.0, sigma_u=0.5, top_ratio=0.05, seed=8)
+    d = Dev(inp, dev)
+    for it in (0, 1):
+        tok, lp = d.run(31, it)
+        compare(inp, tok, lp, oracle_cells(inp, 31, it), label="hot it%d" % it)
+    assert int(d.status.item()) == 0

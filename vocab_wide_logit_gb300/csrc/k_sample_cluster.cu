@@ -277,10 +277,9 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
   }
   const long long P_u = s_Pu;
 
-  for (long long cell = cluster_id; cell < n_cells; cell += n_clusters) {
-    // In fix-up mode only the cells the streaming kernel marked are processed;
-    // every CTA of the cluster reads the same marker before any barrier.
-    if (only_marked && a.out_tokens[cell] != kStreamMark) continue;
+  // One cell, every CTA of the cluster in lock step (all branching around a
+  // cluster barrier depends only on cluster-wide values).
+  auto process = [&](long long cell) {
     const int c = (int)(cell / P);
     const int p = (int)(cell - (long long)c * P);
     if (wid == 0) {
@@ -299,7 +298,7 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
         report(a.d_status, (!(tau >= 0.f) || isnan(g)) ? DS_DEV_ERR_PARAM : DS_DEV_ERR_NO_UNCOND);
       }
       __syncthreads();
-      continue;
+      return;
     }
     const bool guided = g != 0.f;
     const bool sampled = tau > 0.f;
@@ -414,7 +413,7 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
           a.out_logprobs[cell] = __int_as_float(0x7fc00000);
         }
         __syncthreads();
-        continue;
+        return;
       }
       if (sampled && v[0] >= 64 && a.q_lo > -kInf) {
         mu = f[1] / (float)v[0];
@@ -469,7 +468,7 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
           a.out_logprobs[cell] = m - lse;
         }
         __syncthreads();
-        continue;
+        return;
       }
     }
 
@@ -646,6 +645,24 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
       a.out_logprobs[cell] = zw - lse;
     }
     __syncthreads();
+    };
+  if (only_marked) {
+    // Fix-up mode: only the cells the streaming kernel marked. Each round, the
+    // CTA reads NT of its cells' markers at once and lists the marked ones in
+    // slot order (a block scan), so every CTA of the cluster walks the same list.
+    __shared__ long long s_list[NT];
+    for (long long sb = 0; cluster_id + n_clusters * sb < n_cells; sb += NT) {
+      const long long cj = cluster_id + n_clusters * (sb + tid);
+      const int flag = (cj < n_cells && a.out_tokens[cj] == kStreamMark) ? 1 : 0;
+      int total = 0;
+      const int pos = block_excl_scan<NT>(wsum, flag, total);
+      if (flag) s_list[pos] = cj;
+      __syncthreads();
+      for (int i = 0; i < total; ++i) process(s_list[i]);
+      __syncthreads();
+    }
+  } else {
+    for (long long cell = cluster_id; cell < n_cells; cell += n_clusters) process(cell);
   }
   cl.sync();  // no CTA leaves while a peer may still read its exchange slots
 }

@@ -123,7 +123,7 @@ constexpr int kStreamNT = 256;
 constexpr int kStreamUnroll = 2;
 
 template <int NT, int UNROLL>
-__global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, int chunk_cap, int cap) {
+__global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int chunk_cap, int cap) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float2* cand = reinterpret_cast<float2*>(smem_raw);           // [cap] (z, id bits)
   uint16_t* cmax = reinterpret_cast<uint16_t*>(cand + cap);     // [chunk_cap] chunk maxima, bf16 rounded up

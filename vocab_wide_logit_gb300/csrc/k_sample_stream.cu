@@ -1,29 +1,38 @@
 // k_sample_stream.cu -- sampling pass for large vocabularies, streaming form:
 // one thread-block cluster per cell, the row split across its CTAs, each logit
-// read once from HBM; only per-chunk maxima and a few candidates stay on chip.
+// read once from HBM, and the Gumbel race run inside that single pass.
 //
 // Per cell, in each CTA:
-//   pass 1  stream the slice in 16-byte chunks: z = c + g (c - u), an online
-//           (max, sum of exp(z - max), first argmax) per thread rescaled once
-//           per batch, and an upper bound (bf16, rounded up) of every
-//           8-element chunk's max into shared memory
-//   R1      cluster merge of the triples ("perf: avoid full-vocab all-gather for
-//           draft greedy sampling", LightLLM PR #1517, Design and invariants:
-//           per-shard max, log-sum-exp and argmax, ties to the smallest id)
-//   bound   the argmax element's lower-bound score SA = m + tau * G_lo(its
-//           noise) is a score some element reaches, so nothing with
-//           z + tau * G_max < SA can win the Gumbel race ("Sampler support for
-//           discrete diffusion", Hert4's first comment): zmin = SA - tau * G_max
-//   pass 2  re-read (from L2) only the chunks whose max reaches zmin and keep
-//           their elements with z >= zmin as candidates
-//   R3      race over the candidates with table bounds on G, cluster top-2 by
-//           upper bound and C = count(z >= zmin); when C <= k every candidate
-//           ranks inside the kept set (the k largest z, ties to the smallest
-//           id) and every kept element below zmin cannot win, so the race is
-//           exact without forming the kept set
-//   R4      (only when the bounds leave several candidates) exact G for those
-// A cell this cannot settle (C > k or a full candidate buffer) is marked in
-// out_tokens and finished exactly by the staged kernel launched right after.
+//   pass    stream the slice in 16-byte chunks: z = c + g (c - u) and an online
+//           (max, sum of exp(z - max), first argmax) per thread, rescaled once
+//           per batch of chunks
+//   cut     S* (the best perturbed score z + tau G of the whole row) is at least
+//           SA, the best lower-bound score z + tau G_lo found so far, and at
+//           least m + tau G_min for any z = m already seen; G <= G_max for
+//           every noise word, so nothing with z < SA - tau G_max can win
+//           ("Sampler support for discrete diffusion", Hert4's first comment:
+//           Gumbel-max over the kept set). SA is shared by the cluster's CTAs
+//           through atomics on each other's shared memory.
+//   stage   chunks whose max reaches the cut are copied (as 8 z values) to a
+//           per-warp queue in shared memory; each full queue is expanded into
+//           its elements that still reach the cut, and those get their noise
+//           word and table bounds (lo, hi) on G, and raise SA
+//   live    an element whose upper-bound score reaches SA stays on a short
+//           per-warp list; every other element is out of the race
+//   R1      one cluster merge: (max, sum, first argmax) ("perf: avoid
+//           full-vocab all-gather for draft greedy sampling", LightLLM PR
+//           #1517, Design and invariants: per-shard max, log-sum-exp and
+//           argmax, ties to the smallest id), the live lists' best lower
+//           bound S and two best upper bounds, and E, the number of elements
+//           that got noise
+//   R4      (only when the bounds leave two live elements in reach) exact G
+//           for the live elements
+// The race so decided is over the whole row. Its winner w ranks inside the
+// kept set (the k largest z, ties to the smallest id) when E <= k: every
+// element with z >= z_w got noise, so rank(w) <= E, and the whole-row winner
+// is then also the kept-set winner. A cell that fails this (or fills a live
+// list) is marked in out_tokens and finished exactly by the staged kernel
+// launched right after.
 #include <cfloat>
 #include <climits>
 #include <cooperative_groups.h>
@@ -48,19 +57,33 @@ struct SXchg {
   SRec comb;
 };
 
+// Per-warp queues in shared memory.
+constexpr int kStageCap = 96;   // staged chunks: up to 31 left + 2 chunks x 32 lanes per batch
+constexpr int kElemCap = 288;   // elements awaiting noise: up to 31 left + 32 chunks x 8
+constexpr int kLiveCap = 32;    // evaluated elements still in the race
+
+struct alignas(16) WarpArea {
+  float4 stz[kStageCap][2];  // a staged chunk's 8 z values
+  int stq[kStageCap];        // its chunk index
+  float2 eq[kElemCap];       // (z, id bits) awaiting noise
+  float4 live[kLiveCap];     // (z, id bits, lower score, upper score)
+};
+
 __device__ __forceinline__ float max3s(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 
-// Smallest bf16 value >= f (f finite or -inf): an upper bound kept in 16 bits.
-__device__ __forceinline__ uint16_t bf16_ceil(float f) {
-  const uint32_t b = __float_as_uint(f);
-  uint32_t hi = b >> 16;
-  if ((b & 0xffffu) != 0u) hi += (b & 0x80000000u) ? 0u : 1u;  // positive: round up; negative: truncation rounds up
-  return (uint16_t)hi;
+// Order-preserving int image of a float (finite or -inf) for atomicMax.
+__device__ __forceinline__ int ord_enc(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : (i ^ 0x7fffffff);
 }
+__device__ __forceinline__ float ord_dec(int i) { return __int_as_float(i >= 0 ? i : (i ^ 0x7fffffff)); }
+
+// Rounding allowance of a perturbed score near S.
+__device__ __forceinline__ float score_eps(float S) { return (fabsf(S) + 1.f) * 0x1p-20f; }
 
 // Online (max, sum of exp(x - max), first argmax) merge.
 __device__ __forceinline__ void msa_merge(float& m, float& s, int& am, float m2, float s2, int am2) {
@@ -74,6 +97,19 @@ __device__ __forceinline__ void msa_merge(float& m, float& s, int& am, float m2,
   s = s * ex2_approx((m - mm) * kLog2e) + s2 * ex2_approx((m2 - mm) * kLog2e);
   am = (m > m2) ? am : ((m2 > m) ? am2 : min(am, am2));
   m = mm;
+}
+
+// Two best upper bounds (hA from element idA with z = zA; hB the runner-up),
+// ties on hA to the smaller id.
+__device__ __forceinline__ void top2_merge(float& hA, float& hB, float& zA, int& idA, float hA2, float hB2, float zA2,
+                                           int idA2) {
+  const bool take = hA2 > hA || (hA2 == hA && idA2 >= 0 && (idA < 0 || idA2 < idA));
+  hB = fmaxf(fmaxf(hB, hB2), take ? hA : hA2);
+  if (take) {
+    hA = hA2;
+    zA = zA2;
+    idA = idA2;
+  }
 }
 
 // Cluster-wide reduction of one record per CTA. Each warp passes a record already
@@ -123,14 +159,12 @@ constexpr int kStreamNT = 256;
 constexpr int kStreamUnroll = 2;
 
 template <int NT, int UNROLL>
-__global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int chunk_cap, int cap) {
+__global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  float2* cand = reinterpret_cast<float2*>(smem_raw);           // [cap] (z, id bits)
-  uint16_t* cmax = reinterpret_cast<uint16_t*>(cand + cap);     // [chunk_cap] chunk maxima, bf16 rounded up
-  uint16_t* hot = cmax + chunk_cap;                             // [chunk_cap] chunks to revisit
   __shared__ SXchg xs;
   __shared__ SRec wrec[NT / 32];
-  __shared__ int s_nhot, s_ncand;
+  __shared__ float2 s_anc[NT / 32];
+  __shared__ int s_sa[2];  // best lower-bound score of the cell, per cell parity (ord_enc)
   __shared__ ReqCursor s_cur;
   __shared__ long long s_Pu;
   __shared__ int s_bad;
@@ -139,6 +173,8 @@ __global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int
   const int cs = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  WarpArea& W = reinterpret_cast<WarpArea*>(smem_raw)[wid];
   const long long n_cells = (long long)a.C * a.P;
   const long long n_clusters = (long long)gridDim.x / cs;
   const long long cluster_id = (long long)blockIdx.x / cs;
@@ -154,6 +190,10 @@ __global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int
       s_Pu = bt.tot_u;
     }
   }
+  if (tid == 0) {
+    s_sa[0] = ord_enc(-kInf);
+    s_sa[1] = ord_enc(-kInf);
+  }
   __syncthreads();
   if (s_bad) {
     if (rank == 0 && tid == 0) {
@@ -165,22 +205,25 @@ __global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int
     }
     return;  // uniform across the cluster; no shared memory was shared yet
   }
+  cl.sync();  // peers may write s_sa from here on
   const long long P_u = s_Pu;
-  // every G lies below g_max, the upper bound of the last table bucket
+  // every G lies in [g_min, g_max], the outer bounds of the table
   const float g_max = kGumbelBounds[(1u << (32 - DS_GUMBEL_BUCKET_SHIFT)) - 1].y;
+  const float g_min = kGumbelBounds[0].x;
 
-  for (long long cell = cluster_id; cell < n_cells; cell += n_clusters) {
+  int it = 0;
+  for (long long cell = cluster_id; cell < n_cells; cell += n_clusters, ++it) {
     const int c = (int)(cell / P);
     const int p = (int)(cell - (long long)c * P);
+    const int slot = it & 1;
     if (wid == 0) {
       ReqCursor cur;
       warp_find_request(a, p, lane, cur);
-      if (lane == 0) {
-        s_cur = cur;
-        s_nhot = 0;
-        s_ncand = 0;
-      }
+      if (lane == 0) s_cur = cur;
     }
+    // The other parity's slot is next used by the next cell. Peers write it only
+    // after they pass this cell's merge, which waits for this CTA.
+    if (tid == 0) s_sa[slot ^ 1] = ord_enc(-kInf);
     __syncthreads();
     const ReqCursor cur = s_cur;
     const int t = p - cur.off;
@@ -197,6 +240,9 @@ __global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int
     const bool guided = g != 0.f;
     const bool sampled = tau > 0.f;
     const float2 g2 = make_float2(g, g);
+    const uint32_t t32 = (uint32_t)t;
+    const uint32_t ctr3 = a.iter_hi | (uint32_t)c;
+    const float tgmax = tau * g_max;
 
     // ---- slice geometry
     const uint16_t* crow = a.c + cell * (long long)V;
@@ -215,31 +261,7 @@ __global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int
       ub = reinterpret_cast<const uint4*>(ua & ~(uintptr_t)15);
       u_aligned = (ua & 15) == (ca & 15);
     }
-    // z of one 16-byte chunk (ids 8q - dc .. 8q - dc + 7), -inf outside the row
-    auto chunk_z = [&](int q, uint4 vcw, uint4 vuw, float2 (&z)[4]) {
-      const uint32_t wc[4] = {vcw.x, vcw.y, vcw.z, vcw.w};
-      const uint32_t wu[4] = {vuw.x, vuw.y, vuw.z, vuw.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 cp = make_float2(bf_lo(wc[i]), bf_hi(wc[i]));
-        if (guided) {
-          const float2 up = make_float2(bf_lo(wu[i]), bf_hi(wu[i]));
-          z[i] = __ffma2_rn(g2, __ffma2_rn(up, neg1, cp), cp);  // fl(c - u), then one fma
-        } else {
-          z[i] = cp;
-        }
-      }
-      if (q == 0 || q >= nq - 1) {  // row edges
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int id = 8 * q - dc + 2 * i;
-          if (id < 0 || id >= V) z[i].x = -kInf;
-          if (id + 1 < 0 || id + 1 >= V) z[i].y = -kInf;
-        }
-      }
-    };
     auto load_u = [&](int q) -> uint4 {
-      if (!guided) return make_uint4(0u, 0u, 0u, 0u);
       if (u_aligned) return ld_stream16(ub + q);
       const int id0 = 8 * q - dc;
       uint32_t w[4];
@@ -253,29 +275,139 @@ __global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int
       return make_uint4(w[0], w[1], w[2], w[3]);
     };
 
-    // ---- pass 1: stream the slice once. Interior chunks go through full
-    // batches with no per-chunk checks; the row's edge chunks and the last
-    // partial batch go through a checked one-chunk path.
+    // ---- race state (queue lengths and flags are warp-uniform)
     float m = -kInf, s = 0.f;
     int am = INT_MAX;
-    auto pass1 = [&](auto guided_tag) {
-      constexpr bool GD = decltype(guided_tag)::value;
-      // one batch of NCHK chunks at q0, q0 + NT, ...; CHECKED: mask edges and skip q >= q_hi
-      auto load = [&](int q0, auto nchk_tag, auto checked_tag, uint4* vc, uint4* vu) {
+    float SAl = -kInf;           // best lower-bound score this warp knows of
+    int ns = 0, ne = 0, nl = 0;  // staged chunks, queued elements, live elements
+    int E = 0;                   // elements this warp sent to the noise stage
+    bool stop = false;           // cell left to the staged kernel: live list full or E > k
+
+    auto slot_sa = [&]() -> float { return ord_dec(*reinterpret_cast<volatile int*>(&s_sa[slot])); };
+    auto publish = [&](float v) {  // raise SA in every CTA of the cluster
+      if (lane == 0) {
+        const int e = ord_enc(v);
+        for (int r = 0; r < cs; ++r) atomicMax(cl.map_shared_rank(&s_sa[slot], r), e);
+      }
+    };
+    // lowest z that can still win, given the best known score bound and m
+    // (+inf at temperature 0: no race, nothing is staged)
+    auto cut_of = [&](float SA) -> float {
+      const float sb = fmaxf(SA, __fmaf_rn(tau, g_min, m));
+      return (sampled && !stop) ? sb - score_eps(sb) - tgmax : kInf;
+    };
+    // drop live entries whose upper score fell below thr (in place, in order)
+    auto prune = [&](float thr) {
+      int w = 0;
+      for (int b0 = 0; b0 < nl; b0 += 32) {
+        const int i = b0 + lane;
+        const float4 v = (i < nl) ? W.live[i] : make_float4(0.f, 0.f, -kInf, -kInf);
+        const bool keep = i < nl && v.w >= thr;
+        const unsigned bk = __ballot_sync(0xffffffffu, keep);
+        __syncwarp();
+        if (keep) W.live[w + __popc(bk & lt_mask)] = v;
+        w += __popc(bk);
+        __syncwarp();
+      }
+      nl = w;
+    };
+    // noise for the last cnt queued elements; raise SA; keep the ones still in reach
+    auto eval = [&](int cnt) {
+      const int i = ne - cnt + lane;
+      const bool on = lane < cnt;
+      float2 v = make_float2(-kInf, 0.f);
+      float lo = -kInf, hi = -kInf;
+      if (on) {
+        v = W.eq[i];
+        const uint32_t x = noise_word(__float_as_uint(v.y), t32, cur.rid, ctr3, a.rk0, a.rk1);
+        const float2 gb = gumbel_bounds(x);
+        lo = __fmaf_rn(tau, gb.x, v.x);
+        hi = __fmaf_rn(tau, gb.y, v.x);
+      }
+      ne -= cnt;
+      const float wlo = warp_max(lo);
+      const float known = fmaxf(SAl, slot_sa());
+      if (wlo > known) publish(wlo);
+      SAl = fmaxf(known, wlo);
+      const float thr = SAl - score_eps(SAl);
+      const bool lv = on && hi >= thr && hi > -kInf;
+      const unsigned b = __ballot_sync(0xffffffffu, lv);
+      if (b) {
+        if (nl + __popc(b) > kLiveCap) prune(thr);
+        if (nl + __popc(b) > kLiveCap) {
+          stop = true;
+        } else {
+          if (lv) W.live[nl + __popc(b & lt_mask)] = make_float4(v.x, v.y, lo, hi);
+          nl += __popc(b);
+        }
+      }
+      __syncwarp();
+    };
+    // expand the last cnt staged chunks into their elements that reach the cut
+    auto drain = [&](int cnt) {
+      const int e = ns - cnt + lane;
+      const bool on = lane < cnt;
+      float zz[8];
+      int q = 0;
+      if (on) {
+        const float4 A = W.stz[e][0], Bv = W.stz[e][1];
+        zz[0] = A.x; zz[1] = A.y; zz[2] = A.z; zz[3] = A.w;
+        zz[4] = Bv.x; zz[5] = Bv.y; zz[6] = Bv.z; zz[7] = Bv.w;
+        q = W.stq[e];
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) zz[j] = -kInf;
+      }
+      const float cut = cut_of(fmaxf(SAl, slot_sa()));
+      uint32_t mk = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mk |= (zz[j] >= cut && zz[j] > -kInf) ? (1u << j) : 0u;
+      const int n = __popc(mk);
+      const int ex = warp_excl_scan(n, lane);
+      const int tot = __shfl_sync(0xffffffffu, ex + n, 31);
+      E += tot;
+      if (E > k) stop = true;  // the cell goes to the staged kernel: stop staging
+      __syncwarp();
+      int pos = ne + ex;
+      const int id0 = 8 * q - dc;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if ((mk >> j) & 1u) W.eq[pos++] = make_float2(zz[j], __int_as_float(id0 + j));
+      ne += tot;
+      ns -= cnt;
+      __syncwarp();
+    };
+    auto work = [&]() {
+      while (ns >= 32) {
+        drain(32);
+        while (ne >= 32) eval(32);
+      }
+    };
+
+    // ---- the pass. Interior chunks go through full batches with no per-chunk
+    // checks; the row's edge chunks and the last partial batch go through a
+    // checked one-chunk path. MODE: 0 statistics, 1 statistics and staging,
+    // 2 staging only. Guidance and temperature are per-cell flags here rather
+    // than template parameters: one copy of the loop keeps register use low.
+    auto pass = [&]() {
+      auto load = [&](int q0, auto nchk_tag, auto checked_tag, bool act, uint4* vc, uint4* vu) {
         constexpr int NCHK = decltype(nchk_tag)::value;
         constexpr bool CHECKED = decltype(checked_tag)::value;
 #pragma unroll
         for (int uu = 0; uu < NCHK; ++uu) {
           const int q = q0 + uu * NT;
-          const bool ok = !CHECKED || q < q_hi;
+          const bool ok = !CHECKED || (act && q < q_hi);
           vc[uu] = ok ? ld_stream16(cb + q) : make_uint4(0u, 0u, 0u, 0u);
-          if (GD) vu[uu] = ok ? load_u(q) : make_uint4(0u, 0u, 0u, 0u);
+          vu[uu] = (ok && guided) ? load_u(q) : make_uint4(0u, 0u, 0u, 0u);
         }
       };
-      auto compute = [&](int q0, auto nchk_tag, auto checked_tag, const uint4* vc, const uint4* vu) {
+      auto compute = [&](int q0, auto nchk_tag, auto checked_tag, auto mode_tag, bool act, const uint4* vc,
+                         const uint4* vu) {
         constexpr int NCHK = decltype(nchk_tag)::value;
         constexpr bool CHECKED = decltype(checked_tag)::value;
+        constexpr int MODE = decltype(mode_tag)::value;
         float2 z[NCHK][4];
+        float cmx[NCHK];
         float bm = -kInf;
 #pragma unroll
         for (int uu = 0; uu < NCHK; ++uu) {
@@ -284,82 +416,144 @@ __global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 cp = make_float2(bf_lo(wc[i]), bf_hi(wc[i]));
-            if (GD) {
-              const uint32_t wu = (i == 0) ? vu[uu].x : (i == 1) ? vu[uu].y : (i == 2) ? vu[uu].z : vu[uu].w;
-              const float2 up = make_float2(bf_lo(wu), bf_hi(wu));
-              z[uu][i] = __ffma2_rn(g2, __ffma2_rn(up, neg1, cp), cp);  // fl(c - u), then one fma
-            } else {
-              z[uu][i] = cp;
-            }
+            const uint32_t wu = (i == 0) ? vu[uu].x : (i == 1) ? vu[uu].y : (i == 2) ? vu[uu].z : vu[uu].w;
+            const float2 up = make_float2(bf_lo(wu), bf_hi(wu));
+            const float2 zg = __ffma2_rn(g2, __ffma2_rn(up, neg1, cp), cp);  // fl(c - u), then one fma
+            z[uu][i] = guided ? zg : cp;
           }
           if (CHECKED) {
+            const bool ok = act && q < q_hi;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int id = 8 * q - dc + 2 * i;
-              if (q >= q_hi || id < 0 || id >= V) z[uu][i].x = -kInf;
-              if (q >= q_hi || id + 1 < 0 || id + 1 >= V) z[uu][i].y = -kInf;
+              if (!ok || id < 0 || id >= V) z[uu][i].x = -kInf;
+              if (!ok || id + 1 < 0 || id + 1 >= V) z[uu][i].y = -kInf;
             }
           }
           float cm = max3s(z[uu][0].x, z[uu][0].y, z[uu][1].x);
           cm = max3s(cm, z[uu][1].y, z[uu][2].x);
           cm = max3s(cm, z[uu][2].y, z[uu][3].x);
-          cm = fmaxf(cm, z[uu][3].y);
-          if (!CHECKED || q < q_hi) cmax[q - q_lo] = bf16_ceil(cm);
-          bm = fmaxf(bm, cm);
+          cmx[uu] = fmaxf(cm, z[uu][3].y);
+          bm = fmaxf(bm, cmx[uu]);
         }
-        if (bm >= m && bm > -kInf) {
-          // a new (or equal) running max: rescale the sum; keep the smallest id
-          // attaining it (chunks are not visited in id order, so take the min)
-          if (bm > m) {
-            s = (m == -kInf) ? 0.f : s * ex2_approx((m - bm) * kLog2e);
-            m = bm;
-            am = INT_MAX;
-          }
-          int aa = INT_MAX;
-#pragma unroll
-          for (int uu = NCHK - 1; uu >= 0; --uu) {
-#pragma unroll
-            for (int i = 3; i >= 0; --i) {
-              const int id = 8 * (q0 + uu * NT) - dc + 2 * i;
-              if (z[uu][i].y == bm) aa = id + 1;
-              if (z[uu][i].x == bm) aa = id;
+        if (MODE != 2) {
+          if (bm >= m && bm > -kInf) {
+            // a new (or equal) running max: rescale the sum; keep the smallest id
+            // attaining it (chunks are not visited in id order, so take the min)
+            if (bm > m) {
+              s = (m == -kInf) ? 0.f : s * ex2_approx((m - bm) * kLog2e);
+              m = bm;
+              am = INT_MAX;
             }
-          }
-          am = min(am, aa);
-        }
-        if (m != -kInf) {
-          const float2 nml = make_float2(-m * kLog2e, -m * kLog2e);
-          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+            int aa = INT_MAX;
 #pragma unroll
-          for (int uu = 0; uu < NCHK; ++uu)
+            for (int uu = NCHK - 1; uu >= 0; --uu) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 tt = __ffma2_rn(z[uu][i], l2e, nml);
-              const float2 ee = make_float2(ex2_approx(tt.x), ex2_approx(tt.y));
-              if (i & 1) acc1 = __fadd2_rn(acc1, ee); else acc0 = __fadd2_rn(acc0, ee);
+              for (int i = 3; i >= 0; --i) {
+                const int id = 8 * (q0 + uu * NT) - dc + 2 * i;
+                if (z[uu][i].y == bm) aa = id + 1;
+                if (z[uu][i].x == bm) aa = id;
+              }
             }
-          s += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+            am = min(am, aa);
+          }
+          if (m != -kInf) {
+            const float2 nml = make_float2(-m * kLog2e, -m * kLog2e);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int uu = 0; uu < NCHK; ++uu)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 tt = __ffma2_rn(z[uu][i], l2e, nml);
+                const float2 ee = make_float2(ex2_approx(tt.x), ex2_approx(tt.y));
+                if (i & 1) acc1 = __fadd2_rn(acc1, ee); else acc0 = __fadd2_rn(acc0, ee);
+              }
+            s += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+          }
         }
-      };
-      // interior chunks [qa, qb): no row edges inside
-      auto batch = [&](int q0, auto nchk_tag, auto checked_tag) {
-        uint4 vc[decltype(nchk_tag)::value], vu[decltype(nchk_tag)::value];
-        load(q0, nchk_tag, checked_tag, vc, vu);
-        compute(q0, nchk_tag, checked_tag, vc, vu);
+        if (MODE != 0) {
+          const float cut = cut_of(fmaxf(SAl, slot_sa()));
+#pragma unroll
+          for (int uu = 0; uu < NCHK; ++uu) {
+            const bool hot = cmx[uu] >= cut && cmx[uu] > -kInf;
+            const unsigned b = __ballot_sync(0xffffffffu, hot);
+            if (hot) {
+              const int pos = ns + __popc(b & lt_mask);
+              W.stz[pos][0] = make_float4(z[uu][0].x, z[uu][0].y, z[uu][1].x, z[uu][1].y);
+              W.stz[pos][1] = make_float4(z[uu][2].x, z[uu][2].y, z[uu][3].x, z[uu][3].y);
+              W.stq[pos] = q0 + uu * NT;
+            }
+            ns += __popc(b);
+          }
+          __syncwarp();
+          work();
+        }
       };
       using UN = std::integral_constant<int, UNROLL>;
       using ONE = std::integral_constant<int, 1>;
-      if (tid == 0 && q_lo == 0 && q_hi > 0) batch(0, ONE{}, std::true_type{});
+      using STATS = std::integral_constant<int, 0>;
+      using BOTH = std::integral_constant<int, 1>;
+      using STAGE = std::integral_constant<int, 2>;
+      auto batch1 = [&](int q, bool act) {  // one checked chunk
+        uint4 vc[1], vu[1];
+        load(q, ONE{}, std::true_type{}, act, vc, vu);
+        compute(q, ONE{}, std::true_type{}, BOTH{}, act, vc, vu);
+      };
+      // row-edge chunk 0 (lane 0 of warp 0; the whole warp takes part in staging)
+      if (wid == 0 && q_lo == 0 && q_hi > 0) batch1(0, lane == 0);
       const int qa = max(q_lo, 1), qb = min(q_hi, nq - 1);
       const int n_full = (qb > qa) ? (qb - qa) / (NT * UNROLL) : 0;
       int q0 = qa + tid;
+      uint4 cc[UNROLL], cu[UNROLL], nc_[UNROLL], nu[UNROLL];
       if (n_full > 0) {
-        // the next batch's loads are in flight while this one is reduced
-        uint4 cc[UNROLL], cu[UNROLL], nc_[UNROLL], nu[UNROLL];
-        load(q0, UN{}, std::false_type{}, cc, cu);
-        for (int b = 0; b < n_full; ++b, q0 += NT * UNROLL) {
-          if (b + 1 < n_full) load(q0 + NT * UNROLL, UN{}, std::false_type{}, nc_, nu);
-          compute(q0, UN{}, std::false_type{}, cc, cu);
+        load(q0, UN{}, std::false_type{}, true, cc, cu);
+        if (n_full > 1) load(q0 + NT * UNROLL, UN{}, std::false_type{}, true, nc_, nu);
+        compute(q0, UN{}, std::false_type{}, STATS{}, true, cc, cu);
+      }
+      if (sampled) {
+        // Anchor: the CTA's best z so far and its lower-bound score seed SA, so
+        // that the first batch is staged against a useful cut.
+        float bz = m;
+        int bi = am;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float z2 = __shfl_xor_sync(0xffffffffu, bz, o);
+          const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (z2 > bz || (z2 == bz && i2 < bi)) {
+            bz = z2;
+            bi = i2;
+          }
+        }
+        if (lane == 0) s_anc[wid] = make_float2(bz, __int_as_float(bi));
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < NT / 32; ++w) {
+          const float2 v = s_anc[w];
+          const int i2 = __float_as_int(v.y);
+          if (v.x > bz || (v.x == bz && i2 < bi)) {
+            bz = v.x;
+            bi = i2;
+          }
+        }
+        if (bz > -kInf) {
+          const uint32_t x = noise_word((uint32_t)bi, t32, cur.rid, ctr3, a.rk0, a.rk1);
+          const float lo = __fmaf_rn(tau, gumbel_bounds(x).x, bz);
+          if (wid == 0) publish(lo);
+          SAl = fmaxf(SAl, lo);
+        }
+        if (n_full > 0) compute(q0, UN{}, std::false_type{}, STAGE{}, true, cc, cu);
+      }
+      if (n_full > 0) {
+#pragma unroll
+        for (int uu = 0; uu < UNROLL; ++uu) {
+          cc[uu] = nc_[uu];
+          cu[uu] = nu[uu];
+        }
+        q0 += NT * UNROLL;
+        for (int b = 1; b < n_full; ++b, q0 += NT * UNROLL) {
+          // the next batch's loads are in flight while this one is reduced
+          if (b + 1 < n_full) load(q0 + NT * UNROLL, UN{}, std::false_type{}, true, nc_, nu);
+          compute(q0, UN{}, std::false_type{}, BOTH{}, true, cc, cu);
 #pragma unroll
           for (int uu = 0; uu < UNROLL; ++uu) {
             cc[uu] = nc_[uu];
@@ -367,17 +561,20 @@ __global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int
           }
         }
       }
-      // the rest of [qa, qb), then the row-edge chunk nq-1, one chunk at a time
-      for (int q = qa + n_full * NT * UNROLL + tid; q < qb; q += NT) batch(q, ONE{}, std::true_type{});
-      if (tid == 0 && nq - 1 >= max(q_lo, 1) && nq - 1 < q_hi) batch(nq - 1, ONE{}, std::true_type{});
+      // the rest of the slice (at most NT * UNROLL chunks, the row-edge chunk
+      // nq-1 included), one checked chunk per thread and round
+#pragma unroll 1
+      for (int r = 0; r < UNROLL; ++r) batch1(qa + n_full * NT * UNROLL + r * NT + tid, true);
+      if (sampled) {
+        if (ns > 0) drain(ns);
+        while (ne > 0) eval(min(ne, 32));
+      }
     };
-    if (guided)
-      pass1(std::true_type{});
-    else
-      pass1(std::false_type{});
+    pass();
 
-    // ---- R1: cluster max, sum and first argmax
-    float lse;
+    // ---- R1: one cluster merge of the statistics and of the race
+    float lse, zw;
+    int idw;
     {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -386,10 +583,34 @@ __global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int
         const int a2 = __shfl_xor_sync(0xffffffffu, am, o);
         msa_merge(m, s, am, m2, s2, a2);
       }
+      // this warp's live list: best lower score, two best upper scores
+      float loMax = -kInf, hA = -kInf, hB = -kInf, zA = 0.f;
+      int idA = -1;
+      if (lane < nl) {
+        const float4 v = W.live[lane];
+        loMax = v.z;
+        hA = v.w;
+        zA = v.x;
+        idA = __float_as_int(v.y);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        loMax = fmaxf(loMax, __shfl_xor_sync(0xffffffffu, loMax, o));
+        const float hA2 = __shfl_xor_sync(0xffffffffu, hA, o);
+        const float hB2 = __shfl_xor_sync(0xffffffffu, hB, o);
+        const float zA2 = __shfl_xor_sync(0xffffffffu, zA, o);
+        const int idA2 = __shfl_xor_sync(0xffffffffu, idA, o);
+        top2_merge(hA, hB, zA, idA, hA2, hB2, zA2, idA2);
+      }
       SRec r{};
-      r.f[0] = m; r.f[1] = s; r.i[0] = am;
-      const SRec R = cluster_combine<NT, 2, 1>(cl, xs, wrec, r, parity, cs, [](SRec& x, const SRec& y) {
+      r.f[0] = m; r.f[1] = s; r.f[2] = loMax; r.f[3] = hA; r.f[4] = hB; r.f[5] = zA;
+      r.i[0] = am; r.i[1] = idA; r.i[2] = E; r.i[3] = stop ? 1 : 0;
+      const SRec R = cluster_combine<NT, 6, 4>(cl, xs, wrec, r, parity, cs, [](SRec& x, const SRec& y) {
         msa_merge(x.f[0], x.f[1], x.i[0], y.f[0], y.f[1], y.i[0]);
+        x.f[2] = fmaxf(x.f[2], y.f[2]);
+        top2_merge(x.f[3], x.f[4], x.f[5], x.i[1], y.f[3], y.f[4], y.f[5], y.i[1]);
+        x.i[2] += y.i[2];
+        x.i[3] |= y.i[3];
       });
       m = R.f[0];
       am = R.i[0];
@@ -402,125 +623,29 @@ __global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int
         __syncthreads();
         continue;
       }
-    }
-    const uint32_t t32 = (uint32_t)t;
-    const uint32_t ctr3 = a.iter_hi | (uint32_t)c;
-    // the argmax element reaches at least SA, so nothing below zmin can win
-    const float SA = __fmaf_rn(tau, gumbel_bounds(noise_word((uint32_t)am, t32, cur.rid, ctr3, a.rk0, a.rk1)).x, m);
-    const float zmin = SA - (fabsf(SA) + 1.f) * 0x1p-20f - tau * g_max;
-
-    // ---- chunks whose max reaches zmin (warp-aggregated list)
-    const int n_loc = q_hi - q_lo;
-    for (int j0 = 0; j0 < n_loc; j0 += NT) {
-      const int j = j0 + tid;
-      const bool h = (j < n_loc) && (__uint_as_float((uint32_t)cmax[j] << 16) >= zmin);
-      const unsigned b = __ballot_sync(0xffffffffu, h);
-      if (b) {
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&s_nhot, __popc(b));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (h) hot[base + __popc(b & ((1u << lane) - 1u))] = (uint16_t)j;
-      }
-    }
-    __syncthreads();
-    // ---- pass 2: revisit those chunks (L2) and keep their elements >= zmin
-    const int nhot = s_nhot;
-    for (int h = tid; h < nhot; h += NT) {
-      const int q = q_lo + hot[h];
-      float2 z[4];
-      chunk_z(q, ld_stream16(cb + q), load_u(q), z);
-      const int id0 = 8 * q - dc;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (z[i].x >= zmin) {
-          const int pos = atomicAdd(&s_ncand, 1);
-          if (pos < cap) cand[pos] = make_float2(z[i].x, __int_as_float(id0 + 2 * i));
-        }
-        if (z[i].y >= zmin) {
-          const int pos = atomicAdd(&s_ncand, 1);
-          if (pos < cap) cand[pos] = make_float2(z[i].y, __int_as_float(id0 + 2 * i + 1));
-        }
-      }
-    }
-    __syncthreads();
-    const int nc_all = s_ncand;
-    const int nc = min(nc_all, cap);
-
-    // ---- R3: the race over the candidates
-    const float2 tau2 = make_float2(tau, tau);
-    float zw;
-    int idw;
-    {
-      float loMax = -kInf, hA = -kInf, hB = -kInf;
-      int iA = -1;
-      for (int i = tid; i < nc; i += NT) {
-        const float2 v = cand[i];
-        const uint32_t x = noise_word(__float_as_uint(v.y), t32, cur.rid, ctr3, a.rk0, a.rk1);
-        const float2 sc = __ffma2_rn(tau2, gumbel_bounds(x), make_float2(v.x, v.x));
-        loMax = fmaxf(loMax, sc.x);
-        const bool gt = sc.y > hA;
-        hB = gt ? hA : fmaxf(hB, sc.y);
-        iA = gt ? i : iA;
-        hA = fmaxf(hA, sc.y);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float lm2 = __shfl_xor_sync(0xffffffffu, loMax, o);
-        const float hA2 = __shfl_xor_sync(0xffffffffu, hA, o);
-        const float hB2 = __shfl_xor_sync(0xffffffffu, hB, o);
-        const int iA2 = __shfl_xor_sync(0xffffffffu, iA, o);
-        loMax = fmaxf(loMax, lm2);
-        const bool take = hA2 > hA || (hA2 == hA && iA2 >= 0 && (iA < 0 || iA2 < iA));
-        hB = fmaxf(fmaxf(hB, hB2), take ? hA : hA2);
-        if (take) {
-          hA = hA2;
-          iA = iA2;
-        }
-      }
-      SRec r{};
-      r.f[0] = loMax;
-      r.f[1] = hA;
-      r.f[2] = hB;
-      r.f[3] = (iA >= 0) ? cand[iA].x : 0.f;
-      r.i[0] = (iA >= 0) ? __float_as_int(cand[iA].y) : -1;
-      r.i[1] = (wid == 0) ? nc_all : 0;  // a CTA-wide value: count it once per CTA
-      r.i[2] = (nc_all > cap) ? 1 : 0;
-      const SRec R = cluster_combine<NT, 4, 3>(cl, xs, wrec, r, parity, cs, [](SRec& x, const SRec& y) {
-        x.f[0] = fmaxf(x.f[0], y.f[0]);
-        const bool take = y.f[1] > x.f[1] || (y.f[1] == x.f[1] && y.i[0] >= 0 && (x.i[0] < 0 || y.i[0] < x.i[0]));
-        x.f[2] = fmaxf(fmaxf(x.f[2], y.f[2]), take ? x.f[1] : y.f[1]);
-        if (take) {
-          x.f[1] = y.f[1];
-          x.f[3] = y.f[3];
-          x.i[0] = y.i[0];
-        }
-        x.i[1] += y.i[1];
-        x.i[2] |= y.i[2];
-      });
-      const float S = R.f[0];
-      // a full buffer, or candidates that may not all rank inside the kept set
-      if (R.i[2] != 0 || R.i[1] > k || !(S > -kInf)) {
+      const float S = R.f[2];
+      // a full live list, or a winner that may rank outside the kept set
+      if (R.i[3] != 0 || R.i[2] > k || !(S > -kInf)) {
         if (rank == 0 && tid == 0) a.out_tokens[cell] = kStreamMark;
         __syncthreads();
         continue;
       }
-      const float thr = S - (fabsf(S) + 1.f) * 0x1p-20f;
-      if (R.f[2] < thr) {
-        zw = R.f[3];
-        idw = R.i[0];
+      const float thr = S - score_eps(S);
+      if (R.f[4] < thr) {
+        zw = R.f[5];
+        idw = R.i[1];
       } else {
-        // R4: exact G for every candidate whose upper bound reaches thr
+        // R4: exact G for the live elements whose upper score reaches thr
         float bs = -kInf, bz = 0.f;
         int bid = INT_MAX;
-        for (int i = tid; i < nc; i += NT) {
-          const float2 v = cand[i];
-          const int id = __float_as_int(v.y);
-          const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.rk0, a.rk1);
-          if (__fmaf_rn(tau, gumbel_bounds(x).y, v.x) >= thr) {
-            const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
-            if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
-              bs = scr; bz = v.x; bid = id;
-            }
+        if (lane < nl) {
+          const float4 v = W.live[lane];
+          if (v.w >= thr) {
+            const int id = __float_as_int(v.y);
+            const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.rk0, a.rk1);
+            bs = __fmaf_rn(tau, gumbel_accurate(x), v.x);
+            bz = v.x;
+            bid = id;
           }
         }
         const int wl = warp_argmax_lane(bs, bid);
@@ -541,7 +666,7 @@ __global__ void __launch_bounds__(NT, 4) k_sample_stream(const SampleArgs a, int
     }
     __syncthreads();
   }
-  cl.sync();  // no CTA leaves while a peer may still read its exchange slots
+  cl.sync();  // no CTA leaves while a peer may still read its exchange slots or write s_sa
 }
 
 // ---------------------------------------------------------------- launcher
@@ -550,11 +675,8 @@ cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
   // up to 4 CTAs per row: enough logits per thread to amortise the per-cell rounds
   int cs = 1;
   while (cs < 4 && nq_max / cs > 2 * kStreamNT * kStreamUnroll) cs *= 2;
-  const int chunk_cap = (nq_max + cs - 1) / cs + 1;
-  if (chunk_cap > 65535) return cudaErrorInvalidValue;
-  const int cap = 4096;
   auto kern = k_sample_stream<kStreamNT, kStreamUnroll>;
-  const size_t smem = (size_t)cap * sizeof(float2) + (size_t)chunk_cap * 2 * sizeof(uint16_t) + 16;
+  const size_t smem = sizeof(WarpArea) * (kStreamNT / 32);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -577,7 +699,7 @@ cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
   long long n_clusters = max_clusters;
   if (n_clusters > n_cells) n_clusters = n_cells;
   cfg.gridDim = dim3((unsigned)(n_clusters * cs), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, a, chunk_cap, cap);
+  e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

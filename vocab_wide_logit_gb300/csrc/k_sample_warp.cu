@@ -36,7 +36,8 @@ template <int NCH>
 struct WarpSmem {
   float2 col[NCH * 8 + 1][32];  // per-lane candidate columns: (z, id as int bits)
   float2 dense[kDenseCap];      // balanced candidate list
-  int hist[256];                // radix histogram of the exact fallback
+  float hs[kDenseCap];          // upper-bound score of each dense candidate
+  int hist[256];                // radix histogram of the exact fallback; overlap list of the race
 };
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -194,9 +195,13 @@ __device__ __forceinline__ int rank_of(Get get, int n_it, float zw, int idw) {
 }
 
 // The race over a balanced candidate list (the common case): table bounds for
-// two candidates per lane and iteration, branch-free top-2 by upper bound.
-__device__ __forceinline__ float2 race_dense(const SampleArgs& a, const float2* dense, int ctot, int k, float tau,
-                                             uint32_t t32, uint32_t rid, uint32_t ctr3, int lane, int* hist) {
+// two candidates per lane and iteration, branch-free top-2 by upper bound, and
+// each upper score kept in shared memory. When the bounds do not settle the
+// winner, the candidates whose upper score reaches the best lower score are
+// gathered by ballot (usually two or three) and only they get exact G.
+__device__ __forceinline__ float2 race_dense(const SampleArgs& a, const float2* dense, float* hs, int ctot, int k,
+                                             float tau, uint32_t t32, uint32_t rid, uint32_t ctr3, int lane,
+                                             int* hist) {
   const float2 tau2 = make_float2(tau, tau);
   float loMax = -kInf, hA = -kInf, hB = -kInf;
   int iA = 0;
@@ -211,6 +216,8 @@ __device__ __forceinline__ float2 race_dense(const SampleArgs& a, const float2* 
     float2 s1 = __ffma2_rn(tau2, gumbel_bounds(x1), make_float2(v1.x, v1.x));
     s0 = ok0 ? s0 : make_float2(-kInf, -kInf);
     s1 = ok1 ? s1 : make_float2(-kInf, -kInf);
+    if (ok0) hs[i0] = s0.y;
+    if (ok1) hs[i1] = s1.y;
     loMax = fmaxf(loMax, fmaxf(s0.x, s1.x));
     bool gt = s0.y > hA;
     hB = gt ? hA : fmaxf(hB, s0.y);
@@ -238,7 +245,34 @@ __device__ __forceinline__ float2 race_dense(const SampleArgs& a, const float2* 
     if (__popc(bc) == 1 && !cplx) {
       w = dense[__shfl_sync(0xffffffffu, iA, __ffs(bc) - 1)];
     } else {
-      w = race_resolve(a, get, n_it, thr, tau, t32, rid, ctr3);
+      // gather the candidates still in reach, then exact G for each
+      __syncwarp();
+      int nov = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int i = lane + 32 * it;
+        const bool in = i < ctot && hs[i] >= thr;
+        const unsigned b = __ballot_sync(0xffffffffu, in);
+        if (in && nov + __popc(b & ((1u << lane) - 1u)) < 256) hist[nov + __popc(b & ((1u << lane) - 1u))] = i;
+        nov += __popc(b);
+      }
+      __syncwarp();
+      nov = min(nov, 256);
+      float bs = -kInf, bz = 0.f;
+      int bid = INT_MAX;
+      for (int o = lane; o < nov; o += 32) {
+        const float2 v = dense[hist[o]];
+        const int id = __float_as_int(v.y);
+        const uint32_t x = noise_word((uint32_t)id, t32, rid, ctr3, a.rk0, a.rk1);
+        const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
+        if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
+          bs = scr;
+          bid = id;
+          bz = v.x;
+        }
+      }
+      const int wl = warp_argmax_lane(bs, bid);
+      w = make_float2(__shfl_sync(0xffffffffu, bz, wl), __int_as_float(__shfl_sync(0xffffffffu, bid, wl)));
+      __syncwarp();
     }
     // membership of the winner in the exact top-k
     if (ctot > k && rank_of(get, n_it, w.x, __float_as_int(w.y)) >= k) exact = true;
@@ -603,7 +637,7 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
     const uint32_t rid = G.rid;
     float2 w;
     if (items.dense) {
-      w = race_dense(a, sm.dense, ctot, k, tau, t32, rid, ctr3, lane, sm.hist);
+      w = race_dense(a, sm.dense, sm.hs, ctot, k, tau, t32, rid, ctr3, lane, sm.hist);
     } else {
       w = race_generic<NCH>(a, sm, items, ctot, k, tau, t32, rid, ctr3, lane);
     }

@@ -183,28 +183,80 @@ class GreedyRunner:
     bytes_per_step = property(lambda self: self.g.algorithmic_bytes())
 
 
-def time_steps(runner, steps, warmup, world):
+class DeviceTimer:
+    """CUDA events on the current stream (the stream every launch goes to)."""
+
+    def start(self):
+        torch.cuda.synchronize()
+        self.e0 = torch.cuda.Event(enable_timing=True)
+        self.e1 = torch.cuda.Event(enable_timing=True)
+        self.e0.record(torch.cuda.current_stream())
+
+    def stop(self):
+        self.e1.record(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        return self.e0.elapsed_time(self.e1)
+
+
+class HostTimer:
+    """Wall clock, for the CPU (gloo) test of the multi-rank logic."""
+
+    def start(self):
+        self.t0 = time.perf_counter()
+
+    def stop(self):
+        return (time.perf_counter() - self.t0) * 1e3
+
+
+def max_over_ranks(ms, world, device):
+    """Largest per-rank time of the timed region (rank clocks are independent)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_steps(runner, steps, warmup, world, timer=None, device="cuda"):
+    """W untimed steps, then exactly K timed steps bracketed by a barrier and a device
+    synchronisation on both sides; returns ms per step, the max over ranks."""
+    timer = timer or DeviceTimer()
     for i in range(warmup):
         runner.step(i)
-    torch.cuda.synchronize()
+    if device == "cuda":
+        torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
-    st = torch.cuda.current_stream()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(st)
+    timer.start()
     for i in range(steps):
         runner.step(warmup + i)
-    e1.record(st)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ms = timer.stop()
+    ms = max_over_ranks(ms, world, device)
     if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
         torch.distributed.barrier()
     return ms / steps
+
+
+def launches_per_step(w):
+    """Kernels one ds_sample / ds_greedy_lse call launches (mirrors the library's dispatch:
+    one warp-per-cell kernel up to V = 2055; the streaming kernel plus its fix-up pass when
+    4k <= V; the staged cluster kernel otherwise; one greedy kernel)."""
+    if not hasattr(w, "top_ratio"):
+        return 1
+    if w.V <= 2055:
+        return 1
+    import vocab_wide_logit_gb300 as pkg
+    k = pkg.top_k(w.top_ratio, w.V)
+    return 2 if 4 * k <= w.V else 1
+
+
+def dominant_kernel(w):
+    if not hasattr(w, "top_ratio"):
+        return "k_greedy_lse"
+    if w.V <= 2055:
+        return "k_sample_warp"
+    return "k_sample_stream (+ fix-up k_sample_cluster in the same timed step)" \
+        if launches_per_step(w) == 2 else "k_sample_cluster"
 
 
 def oracle_cpu_rate(inp, max_seconds=10.0, iteration=0):
@@ -269,11 +321,13 @@ def e2e_rate(inp, dev, steps):
     return inp.cells / (ms / 1e3), hs.h2d_bytes(), hs.d2h_bytes()
 
 
-def roofline(bytes_per_step, ms, workload):
+def roofline(bytes_per_step, ms, workload, kernel=None):
+    """achieved = algorithmic bytes of one call / its device time (CUDA events around the
+    call's launches, averaged over the timed steps)."""
     peak, src = hbm_peak()
     ach = bytes_per_step / (ms / 1e3) / 1e9
-    return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "peak_source": src, "unit": "GB/s",
-            "frac": round(ach / peak, 4), "frac_of_8000": round(ach / 8000.0, 4),
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(ach, 1), "peak": peak, "peak_source": src,
+            "unit": "GB/s", "frac": round(ach / peak, 4), "frac_of_8000": round(ach / 8000.0, 4),
             "traffic": committed_traffic(workload), "algorithmic_bytes_per_launch": bytes_per_step}
 
 
@@ -310,8 +364,8 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (no flush)" if not is_greedy else
                    "4 rotating input buffers, 508 MB total > L2",
                    "parallelism": "dp%d (independent cells per rank)" % world},
-        "roofline": roofline(runner.bytes_per_step, ms, wname),
-        "gpu_launches": args.steps,
+        "roofline": roofline(runner.bytes_per_step, ms, wname, dominant_kernel(w)),
+        "gpu_launches": args.steps * launches_per_step(w),
         "clocks": clocks,
     }
     if rank == 0 and not is_greedy:
@@ -342,7 +396,7 @@ def run_ours(args):
                 oms = time_steps(runner, max(10, min(args.steps, 1500)), args.warmup, 1)
                 extra[other] = {"workload": ow.name, "ms_per_step": round(oms, 5),
                                 "units_per_s": round(runner.units / (oms / 1e3), 1),
-                                "roofline": roofline(runner.bytes_per_step, oms, other)}
+                                "roofline": roofline(runner.bytes_per_step, oms, other, dominant_kernel(ow))}
                 del ow
             line["also"] = extra
         print(json.dumps(line), flush=True)

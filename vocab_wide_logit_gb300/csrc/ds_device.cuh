@@ -165,6 +165,15 @@ __device__ __forceinline__ int warp_argmax_lane(float s, int id) {
   return __ffs(m) - 1;
 }
 
+// Programmatic dependent launch. Every kernel of the library is launched so
+// that it may be scheduled while the previous kernel on the stream drains;
+// pdl_wait() blocks until that kernel has completed and its writes are
+// visible, and comes before a kernel's first read of any input. pdl_release()
+// lets the next kernel on the stream begin launching at once (it waits in its
+// own pdl_wait() for this one to finish).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ void report(uint32_t* d_status, uint32_t bits) {
   if (d_status) atomicOr(d_status, bits);
 }

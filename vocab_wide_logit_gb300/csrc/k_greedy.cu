@@ -63,6 +63,8 @@ template <int NT, int UNROLL>
 __global__ void __launch_bounds__(NT, 4) k_greedy_lse(const uint16_t* __restrict__ x, int n, int V,
                                                   float* __restrict__ out_max, float* __restrict__ out_lse,
                                                   int* __restrict__ out_argmax) {
+  pdl_release();
+  pdl_wait();
   __shared__ Triple warp_part[NT / 32];
   __shared__ Triple cta_part;
   cg::cluster_group cluster = cg::this_cluster();
@@ -224,13 +226,15 @@ cudaError_t launch_greedy(const uint16_t* x, int n, int V, float* out_max, float
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, x, n, V, out_max, out_lse, out_argmax);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -234,6 +234,8 @@ __device__ __forceinline__ float max3c(float a, float b, float c) {
 
 template <int NT, int UNROLL>
 __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int slice_cap, int only_marked) {
+  pdl_release();
+  pdl_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* zs = reinterpret_cast<float*>(smem_raw);
   uint16_t* idxs = reinterpret_cast<uint16_t*>(zs + slice_cap);
@@ -694,13 +696,15 @@ cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st, int only
   cfg.blockDim = dim3(kClusterNT, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cfg.gridDim = dim3((unsigned)cs, 1, 1);
   int max_clusters = 0;
   e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);

@@ -160,6 +160,7 @@ constexpr int kStreamUnroll = 2;
 
 template <int NT, int UNROLL>
 __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
+  pdl_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ SXchg xs;
   __shared__ SRec wrec[NT / 32];
@@ -666,6 +667,10 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
     }
     __syncthreads();
   }
+  // The next kernel (the fix-up pass) may start launching only now: this grid
+  // is persistent and sized for an empty GPU, so no dependent grid should take
+  // SM room before its cells are done.
+  pdl_release();
   cl.sync();  // no CTA leaves while a peer may still read its exchange slots or write s_sa
 }
 
@@ -683,13 +688,15 @@ cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
   cfg.blockDim = dim3(kStreamNT, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cfg.gridDim = dim3((unsigned)cs, 1, 1);
   int max_clusters = 0;
   e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);

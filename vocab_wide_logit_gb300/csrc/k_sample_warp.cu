@@ -366,6 +366,8 @@ __device__ __forceinline__ void load_cell(const CellGeo& G, int lane, uint4 (&rc
 template <int NCH>
 __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB : ((NCH <= 6) ? 3 : 2))
     k_sample_warp(const SampleArgs a) {
+  pdl_release();
+  pdl_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   WarpSmem<NCH>& sm = reinterpret_cast<WarpSmem<NCH>*>(smem_raw)[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
@@ -669,7 +671,18 @@ static cudaError_t launch_nch(const SampleArgs& a, cudaStream_t st, int num_sms)
   const long long max_useful = (n_cells + (kWarpKernelThreads / 32) - 1) / (kWarpKernelThreads / 32);
   if (blocks > max_useful) blocks = max_useful;
   if (blocks < 1) blocks = 1;
-  k_sample_warp<NCH><<<(unsigned)blocks, kWarpKernelThreads, smem, st>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(kWarpKernelThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_sample_warp<NCH>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -41,6 +41,8 @@ def lib():
         L.dso_greedy_rows.restype = ctypes.c_int
         L.dso_merge_triples.argtypes = [P, P, P, P, i32, P, P, P]
         L.dso_merge_triples.restype = None
+        L.dso_reveal.argtypes = [P, P, P, P, i32, i32, i32, P, P]
+        L.dso_reveal.restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -148,3 +150,19 @@ def merge_triples(maxes, lses, local_argmax, shard_base):
     lib().dso_merge_triples(_ptr(maxes), _ptr(lses), _ptr(local_argmax), _ptr(shard_base),
                             int(maxes.shape[0]), _ptr(om), _ptr(ol), _ptr(oa))
     return float(om[0]), float(ol[0]), int(oa[0])
+
+
+def reveal(scores, tokens, seq_lens, reveal_counts, canvas):
+    """Confidence ranking and reveal (see dso_reveal): returns (new canvas, revealed flags)."""
+    scores = _c(scores, np.float32)
+    C, P = scores.shape
+    tokens = _c(tokens, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    reveal_counts = _c(reveal_counts, np.int32)
+    out = np.array(canvas, dtype=np.int32, copy=True, order="C")
+    rev = np.zeros((C, P), np.uint8)
+    rc = lib().dso_reveal(_ptr(scores), _ptr(tokens), _ptr(seq_lens), _ptr(reveal_counts),
+                          int(seq_lens.shape[0]), int(C), int(P), _ptr(out), _ptr(rev))
+    if rc != 0:
+        raise OracleError("dso_reveal returned %d" % rc)
+    return out, rev

@@ -308,4 +308,42 @@ void dso_merge_triples(const float* maxes, const double* lses, const int32_t* lo
   *out_argmax = a;
 }
 
+int dso_reveal(const float* scores, const int32_t* tokens, const int32_t* seq_lens,
+               const int32_t* reveal_counts, int32_t B, int32_t C, int32_t P,
+               int32_t* canvas, uint8_t* revealed) {
+  if (B < 0 || C < 0 || P < 0) return DSO_ERR_ARG;
+  int64_t off = 0;
+  for (int32_t r = 0; r < B; ++r) off += seq_lens[r] < 0 ? 0 : seq_lens[r];
+  if (off != P) return DSO_ERR_LAYOUT;
+  off = 0;
+  for (int32_t r = 0; r < B; ++r) {
+    const int64_t T = seq_lens[r] < 0 ? 0 : seq_lens[r];
+    const int64_t n = (int64_t)C * T;
+    // the request's cells in rank order: higher score first, then lower flattened index
+    std::vector<int64_t> f(n);
+    for (int64_t i = 0; i < n; ++i) f[i] = i;
+    auto score_of = [&](int64_t fi) {
+      const int64_t c = fi / (T > 0 ? T : 1), t = fi - c * T;
+      return scores[c * (int64_t)P + off + t];
+    };
+    std::sort(f.begin(), f.end(), [&](int64_t a, int64_t b) {
+      const float sa = score_of(a), sb = score_of(b);
+      if (sa != sb) return sa > sb;
+      return a < b;
+    });
+    int64_t k = reveal_counts[r];
+    if (k < 0) k = 0;
+    if (k > n) k = n;
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t fi = f[i];
+      const int64_t c = fi / T, t = fi - c * T;
+      const int64_t cell = c * (int64_t)P + off + t;
+      if (i < k) canvas[cell] = tokens[cell];
+      if (revealed) revealed[cell] = (uint8_t)(i < k ? 1 : 0);
+    }
+    off += T;
+  }
+  return DSO_OK;
+}
+
 }  // extern "C"

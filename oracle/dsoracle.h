@@ -108,6 +108,21 @@ void dso_merge_triples(const float* maxes, const double* lses, const int32_t* lo
                        const int32_t* shard_base, int32_t n_shards,
                        float* out_max, double* out_lse, int32_t* out_argmax);
 
+/*
+ * Confidence ranking and reveal of one diffusion step, as the caller does it
+ * after sampling ("Sampler support for discrete diffusion", Hert4's first
+ * comment: rank the cells of the flattened canvas by score and commit the top
+ * reveal_count). Per request r (positions [off_r, off_r + T_r) of every row
+ * c), the cells are flattened as f = c * T_r + t; the min(reveal_counts[r],
+ * C * T_r) cells first in the order (score desc, f asc) get
+ * canvas[c][off_r + t] = tokens[c][off_r + t] and revealed = 1; every other
+ * cell of the request keeps its canvas value and gets revealed = 0. A
+ * negative reveal count reveals nothing. revealed may be NULL.
+ */
+int dso_reveal(const float* scores, const int32_t* tokens, const int32_t* seq_lens,
+               const int32_t* reveal_counts, int32_t B, int32_t C, int32_t P,
+               int32_t* canvas, uint8_t* revealed);
+
 #ifdef __cplusplus
 }
 #endif

@@ -120,6 +120,96 @@ ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void
 ds_status ds_greedy_lse(const void* logits, int32_t n, int32_t V, float* out_max, float* out_lse,
                         int32_t* out_argmax, void* stream);
 
+/*
+ * ds_merge_triples -- merge per-shard (max, lse, argmax) triples of a
+ * vocabulary-sharded row into the full-row triple.
+ *
+ * Defined by: "perf: avoid full-vocab all-gather for draft greedy sampling"
+ * (LightLLM PR #1517), Design and invariants: each rank holding a vocab shard
+ * sends three FP32 words per token -- its local max, its local log-sum-exp and
+ * its argmax as a global token id with the integer's bits kept in an FP32
+ * word -- and the merge takes the global max, the token of the shard holding
+ * it (the smallest global id when shards tie), and
+ * lse = m + log(sum over shards of exp(lse_s - m)).
+ *
+ * Arguments:
+ *   triples     device float [n][shards][3]: (max, lse, global argmax bits) per
+ *               token and shard, shard order arbitrary. A shard whose logits
+ *               are all -inf carries max = lse = -inf.
+ *   n, shards   n >= 0 (0: nothing launched), shards >= 1.
+ *   out_max     device float [n]: the largest shard max (exact).
+ *   out_lse     device float [n]: the merged logsumexp (fp32, accurate expf/logf).
+ *   out_argmax  device int32 [n]: the winner's global id; smallest id on ties.
+ *   stream      cudaStream_t.
+ * Returns DS_OK, DS_ERR_INVALID_ARG, DS_ERR_UNSUPPORTED (n * shards * 3 > 2^40)
+ * or DS_ERR_CUDA.
+ */
+ds_status ds_merge_triples(const float* triples, int32_t n, int32_t shards, float* out_max, float* out_lse,
+                           int32_t* out_argmax, void* stream);
+
+/* Output element types of ds_log_softmax. */
+#define DS_DTYPE_F32 0
+#define DS_DTYPE_BF16 1
+
+/*
+ * ds_log_softmax -- the greedy triple of every row plus the dense
+ * log-softmax of bf16 logits [n][V].
+ *
+ * Defined by: the dense fallback path of "perf: avoid full-vocab all-gather
+ * for draft greedy sampling" (LightLLM PR #1517), Design and invariants, for
+ * callers that still need full log-probabilities: out[r][i] = x[r][i] -
+ * logsumexp(x[r]). It runs ds_greedy_lse and then one pass that re-reads the
+ * logits and writes 4 (fp32) or 2 (bf16) bytes per element.
+ *
+ * Arguments:
+ *   logits      device bf16 [n][V], V contiguous, 2-byte alignment.
+ *   n, V        n >= 0 (0: nothing launched), V >= 1.
+ *   out         device [n][V] of out_dtype: fp32 (4-byte aligned) or bf16
+ *               rounded to nearest even (2-byte aligned). A row of all -inf
+ *               logits yields NaN (its logsumexp is -inf).
+ *   out_dtype   DS_DTYPE_F32 or DS_DTYPE_BF16.
+ *   out_max, out_lse, out_argmax  as for ds_greedy_lse.
+ *   stream      cudaStream_t.
+ * Returns DS_OK, DS_ERR_INVALID_ARG or DS_ERR_CUDA.
+ */
+ds_status ds_log_softmax(const void* logits, int32_t n, int32_t V, void* out, int32_t out_dtype, float* out_max,
+                         float* out_lse, int32_t* out_argmax, void* stream);
+
+/*
+ * ds_reveal -- confidence ranking and reveal of one diffusion step.
+ *
+ * Defined by: "Sampler support for discrete diffusion" (mstar issue #267),
+ * Hert4's first comment: after every cell is sampled, the caller ranks the
+ * cells of a request's flattened [C, T] canvas by a confidence score and
+ * commits only the top reveal_count (torch.topk over the flattened scores,
+ * then a scatter). Here the order is score descending, then the flattened
+ * index f = c * T_r + t ascending (the smallest index wins a tie, as the
+ * greedy page's tie rule does for token ids), so exactly
+ * min(reveal_counts[r], C * T_r) cells of request r are committed.
+ *
+ * Arguments (B requests, C rows, P = sum of seq_lens positions, packed as in
+ * ds_sample):
+ *   scores         device float [C][P]: the ranking score of every cell (for
+ *                  example ds_sample's logprob, or the caller's own confidence
+ *                  with its penalties applied). Not NaN; -0 and +0 tie.
+ *   tokens         device int32 [C][P]: the sampled token of every cell.
+ *   seq_lens       device int32 [B] (>= 0; sum == P).
+ *   reveal_counts  device int32 [B]: cells to commit per request; <= 0 commits
+ *                  none, >= C * T_r commits all.
+ *   canvas         device int32 [C][P], in/out: committed cells get their
+ *                  token; every other cell keeps its value.
+ *   revealed       device uint8 [C][P] or NULL: 1 for the cells this call
+ *                  committed, 0 for the others.
+ *   d_status       device uint32 or NULL: DS_DEV_ERR_LAYOUT when seq_lens is
+ *                  negative somewhere or does not sum to P (nothing written).
+ *   stream         cudaStream_t.
+ * Returns DS_OK, DS_ERR_INVALID_ARG, DS_ERR_UNSUPPORTED (C * P >= 2^32) or
+ * DS_ERR_CUDA.
+ */
+ds_status ds_reveal(const float* scores, const int32_t* tokens, const int32_t* seq_lens,
+                    const int32_t* reveal_counts, int32_t B, int32_t C, int32_t P, int32_t* canvas,
+                    uint8_t* revealed, uint32_t* d_status, void* stream);
+
 /* Static description of a status code. Never NULL. */
 const char* ds_status_string(ds_status s);
 

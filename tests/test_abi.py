@@ -78,6 +78,25 @@ def test_host_side_argument_errors(lib):
     assert lib.ds_greedy_lse(None, 3, 10, FAKE, FAKE, FAKE, None) == _lib.DS_ERR_INVALID_ARG
 
 
+def test_merge_and_log_softmax_argument_errors(lib):
+    # ds_merge_triples
+    assert lib.ds_merge_triples(FAKE, 0, 4, FAKE, FAKE, FAKE, None) == _lib.DS_OK
+    assert lib.ds_merge_triples(FAKE, 5, 0, FAKE, FAKE, FAKE, None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_merge_triples(FAKE, -1, 4, FAKE, FAKE, FAKE, None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_merge_triples(None, 5, 4, FAKE, FAKE, FAKE, None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_merge_triples(ctypes.c_void_p(0x100002), 5, 4, FAKE, FAKE, FAKE, None) == _lib.DS_ERR_INVALID_ARG
+    # ds_log_softmax
+    f32, bf16 = _lib.DS_DTYPE_F32, _lib.DS_DTYPE_BF16
+    assert lib.ds_log_softmax(FAKE, 0, 10, FAKE, f32, FAKE, FAKE, FAKE, None) == _lib.DS_OK
+    assert lib.ds_log_softmax(FAKE, 2, 0, FAKE, f32, FAKE, FAKE, FAKE, None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_log_softmax(FAKE, 2, 10, FAKE, 7, FAKE, FAKE, FAKE, None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_log_softmax(FAKE, 2, 10, None, f32, FAKE, FAKE, FAKE, None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_log_softmax(FAKE, 2, 10, ctypes.c_void_p(0x100002), f32, FAKE, FAKE, FAKE,
+                              None) == _lib.DS_ERR_INVALID_ARG  # fp32 output needs 4-byte alignment
+    assert lib.ds_log_softmax(FAKE, 2, 10, ctypes.c_void_p(0x100001), bf16, FAKE, FAKE, FAKE,
+                              None) == _lib.DS_ERR_INVALID_ARG
+
+
 def test_python_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(OSError):
         saved = _lib._lib
@@ -86,3 +105,16 @@ def test_python_binding_fails_loudly_without_library(tmp_path):
             _lib.load(str(tmp_path / "missing.so"))
         finally:
             _lib._lib = saved
+
+
+def test_reveal_argument_errors(lib):
+    f = FAKE
+    assert lib.ds_reveal(f, f, f, f, 2, 0, 10, f, None, None, None) == _lib.DS_OK
+    assert lib.ds_reveal(f, f, f, f, 0, 3, 0, f, None, None, None) == _lib.DS_OK
+    assert lib.ds_reveal(f, f, f, f, 0, 3, 5, f, None, None, None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_reveal(f, f, f, f, -1, 3, 5, f, None, None, None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_reveal(None, f, f, f, 2, 3, 5, f, None, None, None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_reveal(f, f, f, f, 2, 3, 5, None, None, None, None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_reveal(ctypes.c_void_p(0x100002), f, f, f, 2, 3, 5, f, None, None,
+                         None) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_reveal(f, f, f, f, 2, 256, 1 << 24, f, None, None, None) == _lib.DS_ERR_UNSUPPORTED

@@ -20,7 +20,10 @@ DS_DEV_ERR_NO_UNCOND = 2
 DS_DEV_ERR_PARAM = 4
 DS_MAX_VOCAB = 262137
 
-EXPORTED = ("ds_sample", "ds_greedy_lse", "ds_status_string", "ds_top_k")
+EXPORTED = ("ds_sample", "ds_greedy_lse", "ds_status_string", "ds_top_k", "ds_merge_triples", "ds_log_softmax",
+            "ds_reveal")
+DS_DTYPE_F32 = 0
+DS_DTYPE_BF16 = 1
 
 _lib = None
 
@@ -49,6 +52,12 @@ def load(path: str = LIB_PATH):
     L.ds_status_string.restype = ctypes.c_char_p
     L.ds_top_k.argtypes = [f32, i32]
     L.ds_top_k.restype = i32
+    L.ds_merge_triples.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+    L.ds_merge_triples.restype = ctypes.c_int
+    L.ds_log_softmax.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp]
+    L.ds_log_softmax.restype = ctypes.c_int
+    L.ds_reveal.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
+    L.ds_reveal.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -99,4 +108,45 @@ def ds_greedy_lse(logits, out_max, out_lse, out_argmax, n=None, V=None, stream=N
                               _stream(stream))
     if check and rc != DS_OK:
         raise DsError("ds_greedy_lse", rc)
+    return rc
+
+
+def ds_merge_triples(triples, out_max, out_lse, out_argmax, n=None, shards=None, stream=None, check=True):
+    """Call ds_merge_triples: triples float32 [n, shards, 3] (max, lse, global argmax bits)."""
+    if n is None:
+        n, shards = triples.shape[0], triples.shape[1]
+    rc = load().ds_merge_triples(_ptr(triples), int(n), int(shards), _ptr(out_max), _ptr(out_lse),
+                                 _ptr(out_argmax), _stream(stream))
+    if check and rc != DS_OK:
+        raise DsError("ds_merge_triples", rc)
+    return rc
+
+
+def ds_log_softmax(logits, out, out_max, out_lse, out_argmax, out_dtype=None, n=None, V=None, stream=None,
+                   check=True):
+    """Call ds_log_softmax: logits [n, V] bf16; out [n, V] float32 or bfloat16."""
+    import torch
+    if n is None:
+        n, V = logits.shape
+    if out_dtype is None:
+        out_dtype = DS_DTYPE_BF16 if out.dtype == torch.bfloat16 else DS_DTYPE_F32
+    rc = load().ds_log_softmax(_ptr(logits), int(n), int(V), _ptr(out), int(out_dtype), _ptr(out_max),
+                               _ptr(out_lse), _ptr(out_argmax), _stream(stream))
+    if check and rc != DS_OK:
+        raise DsError("ds_log_softmax", rc)
+    return rc
+
+
+def ds_reveal(scores, tokens, seq_lens, reveal_counts, canvas, revealed=None, d_status=None, B=None, C=None,
+              P=None, stream=None, check=True):
+    """Call ds_reveal: scores float32 [C, P], tokens/canvas int32 [C, P], seq_lens/reveal_counts int32 [B],
+    revealed uint8 [C, P] or None."""
+    if C is None:
+        C, P = scores.shape
+    if B is None:
+        B = seq_lens.shape[0]
+    rc = load().ds_reveal(_ptr(scores), _ptr(tokens), _ptr(seq_lens), _ptr(reveal_counts), int(B), int(C),
+                          int(P), _ptr(canvas), _ptr(revealed), _ptr(d_status), _stream(stream))
+    if check and rc != DS_OK:
+        raise DsError("ds_reveal", rc)
     return rc

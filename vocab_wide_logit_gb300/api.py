@@ -72,3 +72,34 @@ def greedy_lse(logits, out_max=None, out_lse=None, out_argmax=None, stream=None)
         out_argmax = torch.empty(n, dtype=torch.int32, device=dev)
     _lib.ds_greedy_lse(logits, out_max, out_lse, out_argmax, stream=stream)
     return out_max, out_lse, out_argmax
+
+
+def merge_triples(triples, stream=None):
+    """Merge per-shard triples float32 [n, shards, 3] -> (max, lse, argmax) per token on the GPU."""
+    n = triples.shape[0]
+    dev = triples.device
+    out_max = torch.empty(n, dtype=torch.float32, device=dev)
+    out_lse = torch.empty(n, dtype=torch.float32, device=dev)
+    out_argmax = torch.empty(n, dtype=torch.int32, device=dev)
+    _lib.ds_merge_triples(triples, out_max, out_lse, out_argmax, stream=stream)
+    return out_max, out_lse, out_argmax
+
+
+def log_softmax(logits, dtype=torch.float32, stream=None):
+    """Dense log-softmax of bf16 logits [n, V] (fp32 or bf16 out) and the per-row (max, lse, argmax)."""
+    n, V = logits.shape
+    dev = logits.device
+    out = torch.empty((n, V), dtype=dtype, device=dev)
+    out_max = torch.empty(n, dtype=torch.float32, device=dev)
+    out_lse = torch.empty(n, dtype=torch.float32, device=dev)
+    out_argmax = torch.empty(n, dtype=torch.int32, device=dev)
+    _lib.ds_log_softmax(logits, out, out_max, out_lse, out_argmax, stream=stream)
+    return out, out_max, out_lse, out_argmax
+
+
+def reveal(scores, tokens, seq_lens, reveal_counts, canvas, stream=None):
+    """Commit the top reveal_counts[r] cells of each request (score desc, flattened index asc) into
+    canvas (in place); returns the uint8 [C, P] flags of the committed cells."""
+    revealed = torch.empty(scores.shape, dtype=torch.uint8, device=scores.device)
+    _lib.ds_reveal(scores, tokens, seq_lens, reveal_counts, canvas, revealed, stream=stream)
+    return revealed

@@ -144,4 +144,47 @@ ds_status ds_greedy_lse(const void* logits, int32_t n, int32_t V, float* out_max
   return e == cudaSuccess ? DS_OK : DS_ERR_CUDA;
 }
 
+ds_status ds_merge_triples(const float* triples, int32_t n, int32_t shards, float* out_max, float* out_lse,
+                           int32_t* out_argmax, void* stream) {
+  if (n < 0 || shards < 1) return DS_ERR_INVALID_ARG;
+  if (n == 0) return DS_OK;
+  if (!triples || !out_max || !out_lse || !out_argmax) return DS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(triples) & 3) != 0) return DS_ERR_INVALID_ARG;
+  if ((long long)n * shards * 3 > (1LL << 40)) return DS_ERR_UNSUPPORTED;
+  const cudaError_t e =
+      ds::launch_merge_triples(triples, n, shards, out_max, out_lse, out_argmax, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+ds_status ds_log_softmax(const void* logits, int32_t n, int32_t V, void* out, int32_t out_dtype, float* out_max,
+                         float* out_lse, int32_t* out_argmax, void* stream) {
+  if (n < 0 || V < 1) return DS_ERR_INVALID_ARG;
+  if (out_dtype != DS_DTYPE_F32 && out_dtype != DS_DTYPE_BF16) return DS_ERR_INVALID_ARG;
+  if (n == 0) return DS_OK;
+  if (!logits || !out || !out_max || !out_lse || !out_argmax) return DS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) & 1) || (reinterpret_cast<uintptr_t>(out) & (out_dtype == DS_DTYPE_F32 ? 3 : 1)))
+    return DS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint16_t* x = static_cast<const uint16_t*>(logits);
+  cudaError_t e = ds::launch_greedy(x, n, V, out_max, out_lse, out_argmax, st);
+  if (e == cudaSuccess) e = ds::launch_log_softmax_write(x, n, V, out_lse, out, out_dtype == DS_DTYPE_BF16, st);
+  return e == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+ds_status ds_reveal(const float* scores, const int32_t* tokens, const int32_t* seq_lens,
+                    const int32_t* reveal_counts, int32_t B, int32_t C, int32_t P, int32_t* canvas,
+                    uint8_t* revealed, uint32_t* d_status, void* stream) {
+  if (B < 0 || C < 0 || P < 0) return DS_ERR_INVALID_ARG;
+  if (C == 0 || (B == 0 && P == 0)) return DS_OK;
+  if (B == 0) return DS_ERR_INVALID_ARG;  // P > 0 positions need an owner
+  if (!scores || !tokens || !seq_lens || !reveal_counts || !canvas) return DS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(scores) | reinterpret_cast<uintptr_t>(tokens) |
+       reinterpret_cast<uintptr_t>(canvas)) & 3)
+    return DS_ERR_INVALID_ARG;
+  if ((long long)C * (long long)P >= (1LL << 32)) return DS_ERR_UNSUPPORTED;
+  const cudaError_t e = ds::launch_reveal(scores, tokens, seq_lens, reveal_counts, B, C, P, canvas, revealed,
+                                          d_status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -9,7 +9,7 @@
 namespace ds {
 
 constexpr int kWarpKernelThreads = 128;
-constexpr int kStreamMark = -2;  // out_tokens marker left by the streaming kernel for the staged one  // 4 warps per CTA, one cell per warp at a time
+constexpr int kStreamMark = -2;  // out_tokens marker left by the streaming kernel for the staged one
 
 // Largest V of the one-warp-per-cell kernel and of the cluster kernel.
 int warp_kernel_max_vocab();
@@ -23,5 +23,12 @@ cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st, int only
 cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st);
 cudaError_t launch_greedy(const uint16_t* x, int n, int V, float* out_max, float* out_lse, int* out_argmax,
                           cudaStream_t st);
+cudaError_t launch_merge_triples(const float* triples, int n, int shards, float* out_max, float* out_lse,
+                                 int* out_argmax, cudaStream_t st);
+cudaError_t launch_reveal(const float* scores, const int32_t* tokens, const int32_t* seq_lens,
+                          const int32_t* reveal_counts, int B, int C, int P, int32_t* canvas, uint8_t* revealed,
+                          uint32_t* d_status, cudaStream_t st);
+cudaError_t launch_log_softmax_write(const uint16_t* x, int n, int V, const float* lse, void* out, bool bf16_out,
+                                     cudaStream_t st);
 
 }  // namespace ds

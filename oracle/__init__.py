@@ -37,6 +37,9 @@ def lib():
         L.dso_sample_cells.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, f32, u64, u32,
                                        P, i64, P, P, P, P, P, P, P, P]
         L.dso_sample_cells.restype = ctypes.c_int
+        L.dso_sample_cells_ex.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, f32, u64, P, u32,
+                                          P, i64, P, P, P, P, P, P, P, P]
+        L.dso_sample_cells_ex.restype = ctypes.c_int
         L.dso_greedy_rows.argtypes = [P, i32, i32, P, i64, P, P, P]
         L.dso_greedy_rows.restype = ctypes.c_int
         L.dso_merge_triples.argtypes = [P, P, P, P, i32, P, P, P]
@@ -88,12 +91,15 @@ class OracleError(RuntimeError):
 
 
 def sample_cells(request_ids, c_bits, u_bits, seq_lens, C, P, V, guidance, temperature,
-                 top_ratio, seed, iteration, cells=None):
+                 top_ratio, seed, iteration, cells=None, top_ratios=None, iterations=None):
     """Run the sampling oracle on the listed cells (all cells when None).
 
     c_bits / u_bits are the raw bf16 bit patterns (uint16) of c_logits [C][P][V] and
-    u_logits [C][P_u][V]. Returns a dict of numpy arrays indexed like `cells`.
+    u_logits [C][P_u][V]. top_ratios / iterations (length B) replace the scalars per
+    request when given. Returns a dict of numpy arrays indexed like `cells`.
     """
+    top_ratios = _c(top_ratios, np.float32) if top_ratios is not None else None
+    iterations = _c(iterations, np.uint32) if iterations is not None else None
     request_ids = _c(request_ids, np.int32)
     seq_lens = _c(seq_lens, np.int32)
     guidance = _c(guidance, np.float32)
@@ -111,14 +117,14 @@ def sample_cells(request_ids, c_bits, u_bits, seq_lens, C, P, V, guidance, tempe
         "argmax": np.zeros(n, np.int32), "top1": np.zeros(n, np.float64),
         "top2": np.zeros(n, np.float64), "thresh_ties": np.zeros(n, np.int32),
     }
-    rc = lib().dso_sample_cells(
+    rc = lib().dso_sample_cells_ex(
         _ptr(request_ids), _ptr(c_bits), _ptr(u_bits), _ptr(seq_lens), B, int(C), int(P), int(V),
-        _ptr(guidance), _ptr(temperature), float(top_ratio), int(seed) & (2**64 - 1),
-        int(iteration), _ptr(cells), n, _ptr(out["tokens"]), _ptr(out["logprobs"]),
+        _ptr(guidance), _ptr(temperature), _ptr(top_ratios), float(top_ratio), int(seed) & (2**64 - 1),
+        _ptr(iterations), int(iteration), _ptr(cells), n, _ptr(out["tokens"]), _ptr(out["logprobs"]),
         _ptr(out["lse"]), _ptr(out["max"]), _ptr(out["argmax"]), _ptr(out["top1"]),
         _ptr(out["top2"]), _ptr(out["thresh_ties"]))
     if rc != 0:
-        raise OracleError("dso_sample_cells returned %d" % rc)
+        raise OracleError("dso_sample_cells_ex returned %d" % rc)
     return out
 
 

@@ -112,13 +112,35 @@ int dso_sample_cells(const int32_t* request_ids, const uint16_t* c_logits,
                      double* out_lse, float* out_max, int32_t* out_argmax,
                      double* out_top1, double* out_top2,
                      int32_t* out_thresh_ties) {
+  return dso_sample_cells_ex(request_ids, c_logits, u_logits, seq_lens, B, C, P, V, guidance, temperature,
+                             nullptr, top_ratio, seed, nullptr, iteration, cells, n_cells, out_tokens,
+                             out_logprobs, out_lse, out_max, out_argmax, out_top1, out_top2, out_thresh_ties);
+}
+
+int dso_sample_cells_ex(const int32_t* request_ids, const uint16_t* c_logits,
+                        const uint16_t* u_logits, const int32_t* seq_lens,
+                        int32_t B, int32_t C, int32_t P, int32_t V,
+                        const float* guidance, const float* temperature,
+                        const float* top_ratios, float top_ratio, uint64_t seed,
+                        const uint32_t* iterations, uint32_t iteration,
+                        const int64_t* cells, int64_t n_cells,
+                        int32_t* out_tokens, double* out_logprobs,
+                        double* out_lse, float* out_max, int32_t* out_argmax,
+                        double* out_top1, double* out_top2,
+                        int32_t* out_thresh_ties) {
   if (B < 0 || C < 0 || P < 0 || V <= 0 || n_cells < 0) return DSO_ERR_ARG;
   if (n_cells == 0) return DSO_OK;
   if (!request_ids || !c_logits || !seq_lens || !guidance || !temperature || !cells ||
       !out_tokens || !out_logprobs)
     return DSO_ERR_ARG;
-  if (!(top_ratio > 0.0f && top_ratio <= 1.0f)) return DSO_ERR_ARG;
-  if (C > 256 || iteration >= (1u << 24)) return DSO_ERR_ARG;
+  if (C > 256) return DSO_ERR_ARG;
+  // per-request kept fraction and iteration (the scalars when no array is given)
+  for (int32_t r = 0; r < B; ++r) {
+    const float ratio = top_ratios ? top_ratios[r] : top_ratio;
+    const uint32_t it = iterations ? iterations[r] : iteration;
+    if (!(ratio > 0.0f && ratio <= 1.0f)) return DSO_ERR_ARG;
+    if (it >= (1u << 24)) return DSO_ERR_ARG;
+  }
 
   // Packing: request r owns positions [off_r, off_r + T_r); u holds only the
   // requests with guidance != 0, in request order.
@@ -131,7 +153,6 @@ int dso_sample_cells(const int32_t* request_ids, const uint16_t* c_logits,
   if (total != P) return DSO_ERR_LAYOUT;
   if (total_u > 0 && u_logits == nullptr) return DSO_ERR_LAYOUT;
   const int64_t P_u = total_u;
-  const int32_t k = dso_top_k(top_ratio, V);
   const uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
   const double ninf = -std::numeric_limits<double>::infinity();
 
@@ -161,6 +182,8 @@ int dso_sample_cells(const int32_t* request_ids, const uint16_t* c_logits,
     const float g = guidance[req.r];
     const float tau = temperature[req.r];
     if (!(tau >= 0.0f) || std::isnan(g)) return DSO_ERR_ARG;
+    const int32_t k = dso_top_k(top_ratios ? top_ratios[req.r] : top_ratio, V);
+    const uint32_t iteration_r = iterations ? iterations[req.r] : iteration;
 
     // Step 1: guided logits z over the full vocabulary.
     const uint16_t* crow = c_logits + ((int64_t)c * P + p) * (int64_t)V;
@@ -219,7 +242,7 @@ int dso_sample_cells(const int32_t* request_ids, const uint16_t* c_logits,
       for (int32_t q = 0; q < k; ++q) {
         const int32_t i = order[(size_t)q];
         const uint32_t ctr[4] = {(uint32_t)i >> 2, (uint32_t)req.t, (uint32_t)request_ids[req.r],
-                                 (iteration << 8) | (uint32_t)c};
+                                 (iteration_r << 8) | (uint32_t)c};
         uint32_t words[4];
         dso_philox4x32_10(ctr, key, words);
         const double G = dso_gumbel(words[i & 3]);

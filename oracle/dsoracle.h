@@ -91,6 +91,26 @@ int dso_sample_cells(const int32_t* request_ids, const uint16_t* c_logits,
                      int32_t* out_thresh_ties);
 
 /*
+ * As dso_sample_cells, with a kept fraction and an iteration per request:
+ * request r uses top_ratios[r] (when top_ratios is not NULL, else top_ratio)
+ * and iterations[r] (when iterations is not NULL, else iteration). The
+ * contract's sample(..., iterations) names iterations in the plural ("Add a
+ * sampler resource for discrete diffusion", Contract); each request's k is
+ * ceilf(ratio_r * V) as for the scalar.
+ */
+int dso_sample_cells_ex(const int32_t* request_ids, const uint16_t* c_logits,
+                        const uint16_t* u_logits, const int32_t* seq_lens,
+                        int32_t B, int32_t C, int32_t P, int32_t V,
+                        const float* guidance, const float* temperature,
+                        const float* top_ratios, float top_ratio, uint64_t seed,
+                        const uint32_t* iterations, uint32_t iteration,
+                        const int64_t* cells, int64_t n_cells,
+                        int32_t* out_tokens, double* out_logprobs,
+                        double* out_lse, float* out_max, int32_t* out_argmax,
+                        double* out_top1, double* out_top2,
+                        int32_t* out_thresh_ties);
+
+/*
  * Greedy oracle over a list of rows of logits bf16 [n][V]: per listed row,
  * max (fp32), logsumexp (double) and argmax (smallest id on ties).
  */

@@ -301,3 +301,45 @@ def test_shard_merge_equals_unsharded():
     m, l, a = oracle.merge_triples(mx, ls, am, bounds[:-1])
     assert m == whole["max"][0] and a == whole["argmax"][0] == 130
     assert abs(l - whole["lse"][0]) < 1e-12
+
+
+# ---------------------------------------------------------------------------- per-request ratio / iteration
+def test_per_request_ratio_and_iteration_equal_separate_scalar_calls():
+    """A batch whose requests carry their own top ratio and iteration gives each request the
+    tokens that a batch of that request alone gives with the scalars (the noise is keyed on the
+    request id and the request-local position, so packing does not matter)."""
+    from vocab_wide_logit_gb300 import workloads as wl
+    C, V = 3, 257
+    seq = np.array([5, 7, 4], np.int32)
+    inp = wl.make_sample_inputs("pr", C, seq, V, [2.0, 0.0, 1.5], [0.9, 1.3, 0.5], 3.0, 1.5, 0.1, seed=9)
+    ratios = np.array([0.02, 0.5, 1.0], np.float32)
+    iters = np.array([0, 17, 123456], np.uint32)
+    c_bits = wl.bf16_bits(inp.c_logits).reshape(C, inp.P, V)
+    u_all = wl.bf16_bits(inp.u_logits).reshape(C, inp.P_u, V)
+    both = oracle.sample_cells(inp.request_ids, c_bits, u_all, seq, C, inp.P, V, inp.guidance,
+                               inp.temperature, 0.1, inp.seed, 0, top_ratios=ratios, iterations=iters)
+    tok = both["tokens"].reshape(C, inp.P)
+    lp = both["logprobs"].reshape(C, inp.P)
+    off, off_u = 0, 0
+    for r in range(3):
+        T = int(seq[r])
+        cs = np.ascontiguousarray(c_bits[:, off:off + T])
+        us = np.ascontiguousarray(u_all[:, off_u:off_u + T]) if inp.guidance[r] != 0 else None
+        one = oracle.sample_cells(inp.request_ids[r:r + 1], cs, us, seq[r:r + 1], C, T, V,
+                                  inp.guidance[r:r + 1], inp.temperature[r:r + 1], float(ratios[r]), inp.seed,
+                                  int(iters[r]))
+        assert np.array_equal(one["tokens"].reshape(C, T), tok[:, off:off + T])
+        assert np.array_equal(one["logprobs"].reshape(C, T), lp[:, off:off + T])
+        off += T
+        if inp.guidance[r] != 0:
+            off_u += T
+    # the iteration and the ratio do change the draw somewhere
+    base = oracle.sample_cells(inp.request_ids, c_bits, u_all, seq, C, inp.P, V, inp.guidance,
+                               inp.temperature, 0.1, inp.seed, 0)
+    assert not np.array_equal(base["tokens"], both["tokens"])
+    with pytest.raises(oracle.OracleError):
+        oracle.sample_cells(inp.request_ids, c_bits, u_all, seq, C, inp.P, V, inp.guidance, inp.temperature,
+                            0.1, inp.seed, 0, top_ratios=np.array([0.1, 0.0, 0.1], np.float32))
+    with pytest.raises(oracle.OracleError):
+        oracle.sample_cells(inp.request_ids, c_bits, u_all, seq, C, inp.P, V, inp.guidance, inp.temperature,
+                            0.1, inp.seed, 0, iterations=np.array([0, 1 << 24, 0], np.uint32))

@@ -99,6 +99,33 @@ ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void
                     uint32_t* d_status, void* stream);
 
 /*
+ * ds_sample_ex -- ds_sample with a kept fraction and an iteration per request.
+ *
+ * Defined by: "Add a sampler resource for discrete diffusion" (mstar PR #290),
+ * Contract, which names the iterations of sample(...) in the plural, and the
+ * per-request configuration of "Sampler support for discrete diffusion",
+ * Hert4's first comment (guidance, temperature and the top-ratio filter are
+ * per-request settings).
+ *
+ * Arguments as for ds_sample, plus:
+ *   top_ratios   device float [B] or NULL. When given, request r keeps
+ *                k_r = ceilf(top_ratios[r] * V) (fp32 product, clamped to
+ *                [1, V]) and top_ratio is ignored; a ratio outside (0, 1]
+ *                makes that request's cells token -1 / logprob NaN and sets
+ *                DS_DEV_ERR_PARAM.
+ *   iterations   device uint32 [B] or NULL. When given, request r's noise uses
+ *                iterations[r] (< 2^24, else as an invalid ratio) and iteration
+ *                is ignored.
+ * With both NULL this is ds_sample. Per-request arrays must be 4-byte aligned.
+ * Returns as ds_sample.
+ */
+ds_status ds_sample_ex(const int32_t* request_ids, const void* c_logits, const void* u_logits,
+                       const int32_t* seq_lens, int32_t B, int32_t C, int32_t P, int32_t V,
+                       const float* guidance, const float* temperature, const float* top_ratios,
+                       float top_ratio, uint64_t seed, const uint32_t* iterations, uint32_t iteration,
+                       int32_t* out_tokens, float* out_logprobs, uint32_t* d_status, void* stream);
+
+/*
  * ds_greedy_lse -- per-row max, logsumexp and argmax of bf16 logits [n][V].
  *
  * Defined by: "perf: avoid full-vocab all-gather for draft greedy sampling"

@@ -118,3 +118,18 @@ def test_reveal_argument_errors(lib):
     assert lib.ds_reveal(ctypes.c_void_p(0x100002), f, f, f, 2, 3, 5, f, None, None,
                          None) == _lib.DS_ERR_INVALID_ARG
     assert lib.ds_reveal(f, f, f, f, 2, 256, 1 << 24, f, None, None, None) == _lib.DS_ERR_UNSUPPORTED
+
+
+def test_sample_ex_argument_errors(lib):
+    f = FAKE
+
+    def ex(ratios=None, ratio=0.1, iters=None, it=0, V=8):
+        return lib.ds_sample_ex(f, f, None, f, 1, 1, 1, V, f, f, ratios, ratio, 0, iters, it, f, f, None, None)
+
+    # the scalars are checked only when no per-request array replaces them
+    assert ex(ratio=0.0) == _lib.DS_ERR_INVALID_ARG
+    assert ex(it=1 << 24) == _lib.DS_ERR_INVALID_ARG
+    assert ex(ratios=ctypes.c_void_p(0x100002), ratio=0.0) == _lib.DS_ERR_INVALID_ARG  # misaligned array
+    assert ex(iters=ctypes.c_void_p(0x100001), it=1 << 24) == _lib.DS_ERR_INVALID_ARG
+    assert ex(V=_lib.DS_MAX_VOCAB + 1) == _lib.DS_ERR_UNSUPPORTED
+    assert lib.ds_sample_ex(f, f, None, f, 1, 0, 1, 8, f, f, None, 0.1, 0, None, 0, f, f, None, None) == _lib.DS_OK

@@ -341,3 +341,47 @@ def test_large_vocab_hot_temperatures_take_the_exact_path():
         tok, lp = d.run(31, it)
         compare(inp, tok, lp, oracle_cells(inp, 31, it), label="hot it%d" % it)
     assert int(d.status.item()) == 0
+
+
+# ------------------------------------------------------------------------------ per-request ratio / iteration
+@pytest.mark.parametrize("V", [1025, 4097, 20000])
+def test_per_request_ratio_and_iteration(V):
+    """ds_sample_ex: each request its own kept fraction and iteration; every sampling kernel
+    (the warp kernel at V <= 2055, the streaming pass with its fix-up above) against the oracle."""
+    dev = _dev()
+    B = 6
+    rng = np.random.Generator(np.random.PCG64(V))
+    seq = rng.integers(3, 40, size=B).astype(np.int32)
+    g = np.array([2.0, 0.0, 1.5, 2.0, 0.0, 1.0], np.float32)
+    tau = np.array([0.9, 0.0, 1.3, 0.7, 2.5, 0.9], np.float32)
+    inp = wl.make_sample_inputs("pr%d" % V, 3, seq, V, g, tau, 3.0, 1.5, 0.1, seed=V + 1)
+    ratios = np.array([0.001, 0.1, 1.0, 0.37, 0.02, 0.8], np.float32)
+    iters = np.array([0, 3, 1234, 16777215, 9, 77], np.uint32)
+    d = Dev(inp, dev)
+    tr = torch.from_numpy(ratios).to(dev)
+    ti = torch.from_numpy(iters.view(np.int32)).to(dev)
+    tok = torch.full((inp.C, inp.P), -7, dtype=torch.int32, device=dev)
+    lp = torch.full((inp.C, inp.P), 7.0, dtype=torch.float32, device=dev)
+    pkg.ds_sample(d.rid, d.c, d.u, d.sl, d.g, d.tau, 0.5, inp.seed, 0, tok, lp, d_status=d.status,
+                  top_ratios=tr, iterations=ti)
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0
+    ref = oracle.sample_cells(inp.request_ids, wl.bf16_bits(inp.c_logits), wl.bf16_bits(inp.u_logits),
+                              inp.seq_lens, inp.C, inp.P, inp.V, inp.guidance, inp.temperature, 0.5, inp.seed, 0,
+                              top_ratios=ratios, iterations=iters)
+    compare(inp, tok.cpu().numpy().reshape(-1), lp.cpu().numpy().reshape(-1), ref, label="per-request V%d" % V)
+
+
+def test_per_request_invalid_ratio_is_reported_per_request():
+    dev = _dev()
+    inp = wl.make_sample_inputs("bad_ratio", 2, [4, 5], 1025, [2.0, 2.0], [0.9, 0.9], 3.0, 1.5, 0.1, seed=3)
+    d = Dev(inp, dev)
+    tr = torch.tensor([0.1, 0.0], dtype=torch.float32, device=dev)  # request 1: invalid
+    tok = torch.zeros((inp.C, inp.P), dtype=torch.int32, device=dev)
+    lp = torch.zeros((inp.C, inp.P), dtype=torch.float32, device=dev)
+    pkg.ds_sample(d.rid, d.c, d.u, d.sl, d.g, d.tau, 0.1, inp.seed, 0, tok, lp, d_status=d.status, top_ratios=tr)
+    torch.cuda.synchronize()
+    assert int(d.status.item()) & pkg.DS_DEV_ERR_PARAM
+    t = tok.cpu().numpy()
+    assert (t[:, 4:] == -1).all() and (t[:, :4] >= 0).all()
+    assert np.isnan(lp.cpu().numpy()[:, 4:]).all()

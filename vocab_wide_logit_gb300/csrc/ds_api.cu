@@ -66,20 +66,22 @@ int32_t ds_top_k(float top_ratio, int32_t V) {
   return (int32_t)k;
 }
 
-ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void* u_logits,
-                    const int32_t* seq_lens, int32_t B, int32_t C, int32_t P, int32_t V,
-                    const float* guidance, const float* temperature, float top_ratio,
-                    uint64_t seed, uint32_t iteration, int32_t* out_tokens, float* out_logprobs,
-                    uint32_t* d_status, void* stream) {
+ds_status ds_sample_ex(const int32_t* request_ids, const void* c_logits, const void* u_logits,
+                       const int32_t* seq_lens, int32_t B, int32_t C, int32_t P, int32_t V,
+                       const float* guidance, const float* temperature, const float* top_ratios,
+                       float top_ratio, uint64_t seed, const uint32_t* iterations, uint32_t iteration,
+                       int32_t* out_tokens, float* out_logprobs, uint32_t* d_status, void* stream) {
   if (B < 0 || C < 0 || P < 0 || V < 1) return DS_ERR_INVALID_ARG;
   if (C > DS_MAX_ROWS) return DS_ERR_INVALID_ARG;
-  if (iteration > DS_MAX_ITERATION) return DS_ERR_INVALID_ARG;
-  if (!(top_ratio > 0.0f) || !(top_ratio <= 1.0f)) return DS_ERR_INVALID_ARG;
+  if (!iterations && iteration > DS_MAX_ITERATION) return DS_ERR_INVALID_ARG;
+  if (!top_ratios && !(top_ratio > 0.0f && top_ratio <= 1.0f)) return DS_ERR_INVALID_ARG;
   if (C == 0 || P == 0) return DS_OK;
   if (B == 0) return DS_ERR_INVALID_ARG;  // P > 0 positions need an owner
   if (!request_ids || !c_logits || !seq_lens || !guidance || !temperature || !out_tokens || !out_logprobs)
     return DS_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(c_logits) & 1) || (reinterpret_cast<uintptr_t>(u_logits) & 1))
+    return DS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(top_ratios) & 3) || (reinterpret_cast<uintptr_t>(iterations) & 3))
     return DS_ERR_INVALID_ARG;
   if (V > DS_MAX_VOCAB || V > ds::cluster_kernel_max_vocab()) return DS_ERR_UNSUPPORTED;
   if ((long long)C * (long long)P * (long long)V > (1LL << 46)) return DS_ERR_UNSUPPORTED;
@@ -98,7 +100,10 @@ ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void
   a.C = C;
   a.P = P;
   a.V = V;
-  a.k = ds_top_k(top_ratio, V);
+  a.ratios = top_ratios;
+  a.iters = iterations;
+  // scalar kept count and threshold guesses (used when no per-request ratios are given)
+  a.k = top_ratios ? 1 : ds_top_k(top_ratio, V);
   // Threshold guesses: aim the candidate count a little above k so that the
   // verified count rarely falls short, and the upper count a little below.
   const double kk = (double)a.k;
@@ -109,7 +114,7 @@ ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void
   a.q_hi = (target_hi < 1.0) ? INFINITY : (float)normal_upper_quantile(target_hi / (double)V);
   a.key0 = (uint32_t)(seed & 0xffffffffull);
   a.key1 = (uint32_t)(seed >> 32);
-  a.iter_hi = iteration << 8;
+  a.iter_hi = iterations ? 0u : (iteration << 8);
   // Philox4x32-10 key schedule: round r uses key + r * (0x9E3779B9, 0xBB67AE85).
   for (int r = 0; r < 10; ++r) {
     a.rk0[r] = a.key0 + (uint32_t)r * 0x9E3779B9u;
@@ -122,15 +127,25 @@ ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void
     const int sms = device_sm_count();
     if (sms <= 0) return DS_ERR_CUDA;
     e = ds::launch_sample_warp(a, st, sms);
-  } else if (4LL * a.k <= (long long)V) {
+  } else if (top_ratios || 4LL * a.k <= (long long)V) {
     // streaming pass; the cells it cannot finish exactly are marked and
-    // finished by the staged kernel right behind it on the same stream
+    // finished by the staged kernel right behind it on the same stream (with
+    // per-request ratios every k is possible, and this pair handles each)
     e = ds::launch_sample_stream(a, st);
     if (e == cudaSuccess) e = ds::launch_sample_cluster(a, st, 1);
   } else {
     e = ds::launch_sample_cluster(a, st, 0);
   }
   return e == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void* u_logits,
+                    const int32_t* seq_lens, int32_t B, int32_t C, int32_t P, int32_t V,
+                    const float* guidance, const float* temperature, float top_ratio,
+                    uint64_t seed, uint32_t iteration, int32_t* out_tokens, float* out_logprobs,
+                    uint32_t* d_status, void* stream) {
+  return ds_sample_ex(request_ids, c_logits, u_logits, seq_lens, B, C, P, V, guidance, temperature, nullptr,
+                      top_ratio, seed, nullptr, iteration, out_tokens, out_logprobs, d_status, stream);
 }
 
 ds_status ds_greedy_lse(const void* logits, int32_t n, int32_t V, float* out_max, float* out_lse,

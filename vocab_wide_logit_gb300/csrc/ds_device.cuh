@@ -32,6 +32,8 @@ struct SampleArgs {
   uint32_t key0, key1;
   uint32_t iter_hi;   // iteration << 8
   uint32_t rk0[10], rk1[10];  // Philox round keys (key + r * Weyl constants), computed on the host
+  const float* ratios;        // per-request top ratio [B] (device) or null: k, q_lo, q_hi above
+  const uint32_t* iters;      // per-request iteration [B] (device) or null: iter_hi above
 };
 
 // ---------------------------------------------------------------- loads

@@ -17,7 +17,57 @@ struct ReqCursor {
   int32_t off_u;   // first row of request r inside u's packed positions
   float g, tau;
   uint32_t rid;
+  int32_t k;         // kept count of the request
+  float q_lo, q_hi;  // N(0,1) quantiles seeding the request's threshold guesses
+  uint32_t iter_hi;  // the request's iteration << 8 (noise counter word 3)
+  uint32_t perr;     // DS_DEV_ERR_PARAM when the request's ratio or iteration is invalid
 };
+
+// Upper-tail N(0,1) quantile of p (P(N > x) = p), for the threshold guesses
+// only: -inf for p >= 1, +inf for p <= 0. Out of line: it runs once per
+// request and cell walk, and its temporaries stay out of the kernels' loops.
+static __device__ __noinline__ float upper_quantile(float p) {
+  if (p >= 1.f) return -__builtin_huge_valf();
+  if (p <= 0.f) return __builtin_huge_valf();
+  return 1.41421356f * erfcinvf(2.f * p);
+}
+
+// The request's kept count, threshold quantiles and noise iteration: its own
+// entries when the call passed per-request arrays, else the call's scalars.
+// k = ceilf(ratio * V) in fp32, clamped to [1, V], as for the scalar; the
+// quantiles aim the candidate count a little above and below k, as the host
+// does for the scalar.
+__device__ __forceinline__ void req_params(const SampleArgs& a, int r, ReqCursor& cur) {
+  cur.perr = 0u;
+  if (a.ratios) {
+    const float ratio = a.ratios[r];
+    if (!(ratio > 0.f && ratio <= 1.f)) {
+      cur.perr = DS_DEV_ERR_PARAM;
+      cur.k = 1;
+      cur.q_lo = -__builtin_huge_valf();
+      cur.q_hi = __builtin_huge_valf();
+    } else {
+      int kk = (int)ceilf(ratio * (float)a.V);
+      kk = kk < 1 ? 1 : (kk > a.V ? a.V : kk);
+      cur.k = kk;
+      const float kf = (float)kk, Vf = (float)a.V;
+      const float spread = 1.5f * sqrtf(kf * (1.f - kf / Vf)) + 0.02f * kf + 4.f;
+      cur.q_lo = (kf + spread >= Vf) ? -__builtin_huge_valf() : upper_quantile((kf + spread) / Vf);
+      cur.q_hi = (kf - spread < 1.f) ? __builtin_huge_valf() : upper_quantile((kf - spread) / Vf);
+    }
+  } else {
+    cur.k = a.k;
+    cur.q_lo = a.q_lo;
+    cur.q_hi = a.q_hi;
+  }
+  if (a.iters) {
+    const uint32_t it = a.iters[r];
+    if (it > DS_MAX_ITERATION) cur.perr = DS_DEV_ERR_PARAM;
+    cur.iter_hi = (it & 0xFFFFFFu) << 8;
+  } else {
+    cur.iter_hi = a.iter_hi;
+  }
+}
 
 // Whole-batch totals, computed by each warp (O(B / 32)).
 struct BatchTotals {
@@ -71,6 +121,7 @@ __device__ __forceinline__ bool warp_find_request(const SampleArgs& a, int p, in
       cur.g = a.guidance[cur.r];
       cur.tau = a.temperature[cur.r];
       cur.rid = (uint32_t)a.request_ids[cur.r];
+      req_params(a, cur.r, cur);
       return true;
     }
     off += warp_sum_i(T);

@@ -233,7 +233,7 @@ __device__ __forceinline__ float max3c(float a, float b, float c) {
 }
 
 template <int NT, int UNROLL>
-__global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int slice_cap, int only_marked) {
+__global__ void __launch_bounds__(NT, 2) k_sample_cluster(const SampleArgs a, int slice_cap, int only_marked) {
   pdl_release();
   pdl_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
   const long long n_cells = (long long)a.C * a.P;
   const long long n_clusters = (long long)gridDim.x / cs;
   const long long cluster_id = (long long)blockIdx.x / cs;
-  const int P = a.P, V = a.V, k = a.k;
+  const int P = a.P, V = a.V;
   const float2 neg1 = make_float2(-1.f, -1.f);
   const float2 l2e = make_float2(kLog2e, kLog2e);
   int parity = 0;
@@ -293,11 +293,12 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
     const ReqCursor cur = s_cur;
     const int t = p - cur.off;
     const float g = cur.g, tau = cur.tau;
-    if (!(tau >= 0.f) || isnan(g) || (g != 0.f && a.u == nullptr)) {
+    const int k = cur.k;
+    if (!(tau >= 0.f) || isnan(g) || cur.perr || (g != 0.f && a.u == nullptr)) {
       if (rank == 0 && tid == 0) {
         a.out_tokens[cell] = -1;
         a.out_logprobs[cell] = __int_as_float(0x7fc00000);
-        report(a.d_status, (!(tau >= 0.f) || isnan(g)) ? DS_DEV_ERR_PARAM : DS_DEV_ERR_NO_UNCOND);
+        report(a.d_status, (!(tau >= 0.f) || isnan(g) || cur.perr) ? DS_DEV_ERR_PARAM : DS_DEV_ERR_NO_UNCOND);
       }
       __syncthreads();
       return;
@@ -417,13 +418,13 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
         __syncthreads();
         return;
       }
-      if (sampled && v[0] >= 64 && a.q_lo > -kInf) {
+      if (sampled && v[0] >= 64 && cur.q_lo > -kInf) {
         mu = f[1] / (float)v[0];
         sd = sqrtf(fmaxf(f[2] / (float)v[0] - mu * mu, 0.f));
-        const float guess = fmaf(sd, a.q_lo, mu);
+        const float guess = fmaf(sd, cur.q_lo, mu);
         if (isfinite(guess)) {
           tlo = fminf(guess, m);
-          const float gh = fmaf(sd, a.q_hi, mu);
+          const float gh = fmaf(sd, cur.q_hi, mu);
           if (isfinite(gh)) thi = gh;
         }
       }
@@ -504,7 +505,7 @@ __global__ void __launch_bounds__(NT) k_sample_cluster(const SampleArgs a, int s
 
     // ---- Gumbel race: table bounds per candidate, cluster-wide top-2 by upper bound
     const uint32_t t32 = (uint32_t)t;
-    const uint32_t ctr3 = a.iter_hi | (uint32_t)c;
+    const uint32_t ctr3 = cur.iter_hi | (uint32_t)c;
     const float2 tau2 = make_float2(tau, tau);
     {
       float loMax = -kInf;

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
   const long long n_cells = (long long)a.C * a.P;
   const long long n_clusters = (long long)gridDim.x / cs;
   const long long cluster_id = (long long)blockIdx.x / cs;
-  const int P = a.P, V = a.V, k = a.k;
+  const int P = a.P, V = a.V;
   const float2 neg1 = make_float2(-1.f, -1.f);
   const float2 l2e = make_float2(kLog2e, kLog2e);
   int parity = 0;
@@ -229,11 +229,11 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
     const ReqCursor cur = s_cur;
     const int t = p - cur.off;
     const float g = cur.g, tau = cur.tau;
-    if (!(tau >= 0.f) || isnan(g) || (g != 0.f && a.u == nullptr)) {
+    if (!(tau >= 0.f) || isnan(g) || cur.perr || (g != 0.f && a.u == nullptr)) {
       if (rank == 0 && tid == 0) {
         a.out_tokens[cell] = -1;
         a.out_logprobs[cell] = __int_as_float(0x7fc00000);
-        report(a.d_status, (!(tau >= 0.f) || isnan(g)) ? DS_DEV_ERR_PARAM : DS_DEV_ERR_NO_UNCOND);
+        report(a.d_status, (!(tau >= 0.f) || isnan(g) || cur.perr) ? DS_DEV_ERR_PARAM : DS_DEV_ERR_NO_UNCOND);
       }
       __syncthreads();
       continue;
@@ -242,7 +242,8 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
     const bool sampled = tau > 0.f;
     const float2 g2 = make_float2(g, g);
     const uint32_t t32 = (uint32_t)t;
-    const uint32_t ctr3 = a.iter_hi | (uint32_t)c;
+    const uint32_t ctr3 = cur.iter_hi | (uint32_t)c;
+    const int k = cur.k;
     const float tgmax = tau * g_max;
 
     // ---- slice geometry

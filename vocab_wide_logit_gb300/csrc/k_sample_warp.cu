@@ -81,6 +81,9 @@ struct CellGeo {
   const uint16_t* urow;
   int h, nfc, ns, sid;
   bool u_vec;         // u row aligned like the c row: vector loads
+  int k;              // the request's kept count
+  float q_lo;         // and its lower threshold quantile
+  uint32_t iter_hi;   // and its iteration << 8
 };
 
 
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
   const long long cend = (gw + 1) * n_cells / nw;
   if (cbeg >= cend) return;
 
-  const int P = a.P, V = a.V, k = a.k;
+  const int P = a.P, V = a.V;
   const BatchTotals bt = warp_batch_totals(a, lane);
   if (bt.bad || bt.tot != (long long)P) {
     for (long long cell = cbeg + lane; cell < cend; cell += 32) {
@@ -412,6 +415,7 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
       cur.g = a.guidance[cur.r];
       cur.tau = a.temperature[cur.r];
       cur.rid = (uint32_t)a.request_ids[cur.r];
+      req_params(a, cur.r, cur);
     }
     CellGeo G;
     G.c = c;
@@ -420,8 +424,11 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
     G.g = cur.g;
     G.tau = cur.tau;
     G.rid = cur.rid;
-    G.err = (!(G.tau >= 0.f) || isnan(G.g)) ? DS_DEV_ERR_PARAM
-                                            : ((G.g != 0.f && a.u == nullptr) ? DS_DEV_ERR_NO_UNCOND : 0u);
+    G.err = (!(G.tau >= 0.f) || isnan(G.g) || cur.perr) ? DS_DEV_ERR_PARAM
+                                                        : ((G.g != 0.f && a.u == nullptr) ? DS_DEV_ERR_NO_UNCOND : 0u);
+    G.k = cur.k;
+    G.q_lo = cur.q_lo;
+    G.iter_hi = cur.iter_hi;
     G.crow = a.c + cell * (long long)V;
     const uintptr_t ca = reinterpret_cast<uintptr_t>(G.crow);
     G.h = min((int)(((16u - (unsigned)(ca & 15)) & 15u) >> 1), V);
@@ -461,6 +468,7 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
       continue;
     }
     const float g = G.g, tau = G.tau;
+    const int k = G.k;
     const bool guided = g != 0.f;
     const int ns = G.ns, sid = G.sid;
 
@@ -552,12 +560,12 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
     // ---- threshold guess from the subsample moments
     float tlo = -FLT_MAX;  // -FLT_MAX: keep every finite element
     bool guessed = false;
-    if (NCH >= 2 && a.q_lo > -kInf) {
+    if (NCH >= 2 && G.q_lo > -kInf) {
       const float inv_n = 1.0f / (float)(32 * 8 * (NCH > 1 ? NCH - 1 : 1));  // power of two: exact
       const float S1 = warp_sum(s1.x + s1.y), S2 = warp_sum(s2.x + s2.y);
       const float mu = S1 * inv_n;
       const float sd = sqrtf(fmaxf(fmaf(S2, inv_n, -mu * mu), 0.f));
-      const float guess = fmaf(sd, a.q_lo, mu);
+      const float guess = fmaf(sd, G.q_lo, mu);
       if (isfinite(guess)) {
         tlo = fminf(guess, m);
         guessed = true;
@@ -635,7 +643,7 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
 
     // ---- step 4: Gumbel race
     const uint32_t t32 = (uint32_t)G.t;
-    const uint32_t ctr3 = a.iter_hi | (uint32_t)G.c;
+    const uint32_t ctr3 = G.iter_hi | (uint32_t)G.c;
     const uint32_t rid = G.rid;
     float2 w;
     if (items.dense) {

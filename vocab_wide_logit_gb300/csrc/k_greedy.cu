@@ -60,7 +60,7 @@ __device__ __forceinline__ float max3g(float a, float b, float c) {
 }
 
 template <int NT, int UNROLL>
-__global__ void __launch_bounds__(NT, 4) k_greedy_lse(const uint16_t* __restrict__ x, int n, int V,
+__global__ void __launch_bounds__(NT, 2) k_greedy_lse(const uint16_t* __restrict__ x, int n, int V,
                                                   float* __restrict__ out_max, float* __restrict__ out_lse,
                                                   int* __restrict__ out_argmax) {
   pdl_release();
@@ -201,7 +201,9 @@ __global__ void __launch_bounds__(NT, 4) k_greedy_lse(const uint16_t* __restrict
 // ---------------------------------------------------------------- launcher
 cudaError_t launch_greedy(const uint16_t* x, int n, int V, float* out_max, float* out_lse, int* out_argmax,
                           cudaStream_t st) {
-  constexpr int NT = 256;
+  // 512 threads, 2 CTAs per SM: measured 25.1 us against 25.8 us for 256 x 4 at
+  // 256 rows x V = 248320
+  constexpr int NT = 512;
   constexpr int UNROLL = 4;
   auto kern = k_greedy_lse<NT, UNROLL>;
   int dev = 0, sms = 0, per_sm = 0;

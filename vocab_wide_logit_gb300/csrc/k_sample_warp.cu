@@ -208,11 +208,22 @@ __device__ __forceinline__ float2 race_dense(const SampleArgs& a, const float2* 
   const float2 tau2 = make_float2(tau, tau);
   float loMax = -kInf, hA = -kInf, hB = -kInf;
   int iA = 0;
+  // the first 128 candidates stay in registers for the rank check below
+  float2 keep[4] = {make_float2(-kInf, 0.f), make_float2(-kInf, 0.f), make_float2(-kInf, 0.f),
+                    make_float2(-kInf, 0.f)};
+#pragma unroll 1
   for (int base = 0; base < ctot; base += 64) {
     const int i0 = base + lane, i1 = i0 + 32;
     const bool ok0 = i0 < ctot, ok1 = i1 < ctot;
     const float2 v0 = dense[ok0 ? i0 : 0];
     const float2 v1 = dense[ok1 ? i1 : 0];
+    if (base == 0) {
+      keep[0] = ok0 ? v0 : make_float2(-kInf, __int_as_float(INT_MAX));
+      keep[1] = ok1 ? v1 : make_float2(-kInf, __int_as_float(INT_MAX));
+    } else if (base == 64) {
+      keep[2] = ok0 ? v0 : make_float2(-kInf, __int_as_float(INT_MAX));
+      keep[3] = ok1 ? v1 : make_float2(-kInf, __int_as_float(INT_MAX));
+    }
     const uint32_t x0 = noise_word(__float_as_uint(v0.y), t32, rid, ctr3, a.rk0, a.rk1);
     const uint32_t x1 = noise_word(__float_as_uint(v1.y), t32, rid, ctr3, a.rk0, a.rk1);
     float2 s0 = __ffma2_rn(tau2, gumbel_bounds(x0), make_float2(v0.x, v0.x));  // (lower, upper) score
@@ -278,7 +289,20 @@ __device__ __forceinline__ float2 race_dense(const SampleArgs& a, const float2* 
       __syncwarp();
     }
     // membership of the winner in the exact top-k
-    if (ctot > k && rank_of(get, n_it, w.x, __float_as_int(w.y)) >= k) exact = true;
+    if (ctot > k) {
+      int rr;
+      if (ctot <= 128) {  // from registers: the candidates this lane held in the race
+        const int idw = __float_as_int(w.y);
+        int c = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          c += (keep[u].x > w.x || (keep[u].x == w.x && __float_as_int(keep[u].y) < idw)) ? 1 : 0;
+        rr = warp_sum_i(c);
+      } else {
+        rr = rank_of(get, n_it, w.x, __float_as_int(w.y));
+      }
+      if (rr >= k) exact = true;
+    }
   }
   if (exact) {
     const unsigned long long kth = (ctot > k) ? kth_key(get, n_it, k, lane, hist) : 0ull;

@@ -128,6 +128,16 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+// Max of a float across the warp in one reduce instruction over an
+// order-preserving integer image; NaN is mapped below -inf, so it never wins
+// (as with fmaxf).
+__device__ __forceinline__ float warp_max_r(float v) {
+  const int i = __float_as_int(v);
+  const int key = (v != v) ? (int)0x807fffff : (i >= 0 ? i : (i ^ 0x7fffffff));
+  const int mx = __reduce_max_sync(0xffffffffu, key);
+  return __int_as_float(mx >= 0 ? mx : (mx ^ 0x7fffffff));
+}
+
 // Integer reductions use the warp-wide reduce instruction (one step instead of five shuffles).
 __device__ __forceinline__ int warp_sum_i(int v) { return __reduce_add_sync(0xffffffffu, v); }
 __device__ __forceinline__ int warp_min_i(int v) { return __reduce_min_sync(0xffffffffu, v); }

@@ -249,7 +249,7 @@ __device__ __forceinline__ float2 race_dense(const SampleArgs& a, const float2* 
     return true;
   };
   const int n_it = (ctot + 31) >> 5;
-  const float S = warp_max(loMax);
+  const float S = warp_max_r(loMax);
   float2 w;
   bool exact = !(S > -kInf);
   if (!exact) {
@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
       const float cf = __uint_as_float(sc << 16);
       zs1 = (lane < ns) ? (guided ? cfg_combine(cf, __uint_as_float(su << 16), g) : cf) : -kInf;
     }
-    const float m = warp_max(max3(m0, m1, zs1));
+    const float m = warp_max_r(max3(m0, m1, zs1));
     if (m == -kInf) {  // every logit is -inf: token 0, logprob NaN
       prefetch_next();
       if (lane == 0) {

@@ -37,7 +37,7 @@ def lib():
         L.dso_sample_cells.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, f32, u64, u32,
                                        P, i64, P, P, P, P, P, P, P, P]
         L.dso_sample_cells.restype = ctypes.c_int
-        L.dso_sample_cells_ex.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, f32, u64, P, u32,
+        L.dso_sample_cells_ex.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, f32, u64, P, u32, u32,
                                           P, i64, P, P, P, P, P, P, P, P]
         L.dso_sample_cells_ex.restype = ctypes.c_int
         L.dso_greedy_rows.argtypes = [P, i32, i32, P, i64, P, P, P]
@@ -91,7 +91,7 @@ class OracleError(RuntimeError):
 
 
 def sample_cells(request_ids, c_bits, u_bits, seq_lens, C, P, V, guidance, temperature,
-                 top_ratio, seed, iteration, cells=None, top_ratios=None, iterations=None):
+                 top_ratio, seed, iteration, cells=None, top_ratios=None, iterations=None, keep_ties=False):
     """Run the sampling oracle on the listed cells (all cells when None).
 
     c_bits / u_bits are the raw bf16 bit patterns (uint16) of c_logits [C][P][V] and
@@ -120,7 +120,8 @@ def sample_cells(request_ids, c_bits, u_bits, seq_lens, C, P, V, guidance, tempe
     rc = lib().dso_sample_cells_ex(
         _ptr(request_ids), _ptr(c_bits), _ptr(u_bits), _ptr(seq_lens), B, int(C), int(P), int(V),
         _ptr(guidance), _ptr(temperature), _ptr(top_ratios), float(top_ratio), int(seed) & (2**64 - 1),
-        _ptr(iterations), int(iteration), _ptr(cells), n, _ptr(out["tokens"]), _ptr(out["logprobs"]),
+        _ptr(iterations), int(iteration), 1 if keep_ties else 0, _ptr(cells), n, _ptr(out["tokens"]),
+        _ptr(out["logprobs"]),
         _ptr(out["lse"]), _ptr(out["max"]), _ptr(out["argmax"]), _ptr(out["top1"]),
         _ptr(out["top2"]), _ptr(out["thresh_ties"]))
     if rc != 0:

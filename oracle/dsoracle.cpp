@@ -113,7 +113,7 @@ int dso_sample_cells(const int32_t* request_ids, const uint16_t* c_logits,
                      double* out_top1, double* out_top2,
                      int32_t* out_thresh_ties) {
   return dso_sample_cells_ex(request_ids, c_logits, u_logits, seq_lens, B, C, P, V, guidance, temperature,
-                             nullptr, top_ratio, seed, nullptr, iteration, cells, n_cells, out_tokens,
+                             nullptr, top_ratio, seed, nullptr, iteration, 0u, cells, n_cells, out_tokens,
                              out_logprobs, out_lse, out_max, out_argmax, out_top1, out_top2, out_thresh_ties);
 }
 
@@ -122,13 +122,15 @@ int dso_sample_cells_ex(const int32_t* request_ids, const uint16_t* c_logits,
                         int32_t B, int32_t C, int32_t P, int32_t V,
                         const float* guidance, const float* temperature,
                         const float* top_ratios, float top_ratio, uint64_t seed,
-                        const uint32_t* iterations, uint32_t iteration,
+                        const uint32_t* iterations, uint32_t iteration, uint32_t flags,
                         const int64_t* cells, int64_t n_cells,
                         int32_t* out_tokens, double* out_logprobs,
                         double* out_lse, float* out_max, int32_t* out_argmax,
                         double* out_top1, double* out_top2,
                         int32_t* out_thresh_ties) {
   if (B < 0 || C < 0 || P < 0 || V <= 0 || n_cells < 0) return DSO_ERR_ARG;
+  if ((flags & ~DSO_KEEP_TIES) != 0u) return DSO_ERR_ARG;
+  const bool keep_ties = (flags & DSO_KEEP_TIES) != 0u;
   if (n_cells == 0) return DSO_OK;
   if (!request_ids || !c_logits || !seq_lens || !guidance || !temperature || !cells ||
       !out_tokens || !out_logprobs)
@@ -229,17 +231,24 @@ int dso_sample_cells_ex(const int32_t* request_ids, const uint16_t* c_logits,
       };
       if (k < V) std::nth_element(order.begin(), order.begin() + (k - 1), order.end(), before);
       // The k-th element of the order sits at position k-1; count ids equal in z to it
-      // that fall outside the kept set (diagnostic only).
+      // that fall outside the kept set (diagnostic only). With keep_ties they are
+      // kept: the kept set grows to every id whose z reaches the k-th largest z.
+      int32_t n_kept = k;
       if (k < V) {
         const float zk = z[(size_t)order[(size_t)(k - 1)]];
         for (int32_t q = k; q < V; ++q)
-          if (z[(size_t)order[(size_t)q]] == zk) ++thresh_ties;
+          if (z[(size_t)order[(size_t)q]] == zk) {
+            if (keep_ties)
+              std::swap(order[(size_t)n_kept++], order[(size_t)q]);
+            else
+              ++thresh_ties;
+          }
       }
       // Step 4: Gumbel-max over the kept set at temperature tau.
       int32_t best = -1;
       top1 = ninf;
       top2 = ninf;
-      for (int32_t q = 0; q < k; ++q) {
+      for (int32_t q = 0; q < n_kept; ++q) {
         const int32_t i = order[(size_t)q];
         const uint32_t ctr[4] = {(uint32_t)i >> 2, (uint32_t)req.t, (uint32_t)request_ids[req.r],
                                  (iteration_r << 8) | (uint32_t)c};

@@ -33,6 +33,9 @@
 extern "C" {
 #endif
 
+/* Flags of dso_sample_cells_ex. */
+#define DSO_KEEP_TIES 1u  /* keep every id whose z equals the k-th largest z (kept set may exceed k) */
+
 /* Return codes. */
 #define DSO_OK 0
 #define DSO_ERR_ARG 1      /* bad sizes, pointers or scalars */
@@ -96,14 +99,17 @@ int dso_sample_cells(const int32_t* request_ids, const uint16_t* c_logits,
  * and iterations[r] (when iterations is not NULL, else iteration). The
  * contract's sample(..., iterations) names iterations in the plural ("Add a
  * sampler resource for discrete diffusion", Contract); each request's k is
- * ceilf(ratio_r * V) as for the scalar.
+ * ceilf(ratio_r * V) as for the scalar. flags: 0, or DSO_KEEP_TIES, which keeps
+ * every id whose z equals the k-th largest z instead of exactly k ids (a filter
+ * mode the pages leave open: "keep the ceil(0.1 V) largest" says nothing of
+ * ties at the cut).
  */
 int dso_sample_cells_ex(const int32_t* request_ids, const uint16_t* c_logits,
                         const uint16_t* u_logits, const int32_t* seq_lens,
                         int32_t B, int32_t C, int32_t P, int32_t V,
                         const float* guidance, const float* temperature,
                         const float* top_ratios, float top_ratio, uint64_t seed,
-                        const uint32_t* iterations, uint32_t iteration,
+                        const uint32_t* iterations, uint32_t iteration, uint32_t flags,
                         const int64_t* cells, int64_t n_cells,
                         int32_t* out_tokens, double* out_logprobs,
                         double* out_lse, float* out_max, int32_t* out_argmax,

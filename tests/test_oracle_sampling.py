@@ -343,3 +343,52 @@ def test_per_request_ratio_and_iteration_equal_separate_scalar_calls():
     with pytest.raises(oracle.OracleError):
         oracle.sample_cells(inp.request_ids, c_bits, u_all, seq, C, inp.P, V, inp.guidance, inp.temperature,
                             0.1, inp.seed, 0, iterations=np.array([0, 1 << 24, 0], np.uint32))
+
+
+# ---------------------------------------------------------------------------- keep-ties filter mode
+def _bf16_bits_of(values):
+    import torch
+    return torch.tensor(values, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_keep_ties_brute_force_on_a_tiny_vocabulary():
+    """Keep-ties mode against a brute-force race built from the pinned Philox and Gumbel
+    primitives: the kept set is every id whose z reaches the k-th largest z."""
+    V, k_ratio = 16, 0.25  # k = 4
+    rng = np.random.Generator(np.random.PCG64(5))
+    key = (123456789, 987)
+    seed = key[0] | (key[1] << 32)
+    for trial in range(40):
+        # few distinct values: the cut often falls inside a run of equal z
+        z = rng.integers(0, 4, size=V).astype(np.float32)
+        bits = _bf16_bits_of(z).reshape(1, 1, V)
+        tau = 0.8
+        rid = 1000 + trial
+        out = oracle.sample_cells([rid], bits, None, [1], 1, 1, V, [0.0], [tau], k_ratio, seed, 3,
+                                  keep_ties=True)
+        zk = np.sort(z)[::-1][oracle.top_k(k_ratio, V) - 1]
+        kept = np.nonzero(z >= zk)[0]
+        best, best_s = None, -np.inf
+        for i in kept:
+            words = oracle.philox4x32_10([i >> 2, 0, rid, (3 << 8) | 0], key)
+            s = float(z[i]) + tau * oracle.gumbel(int(words[i & 3]))
+            if s > best_s:
+                best, best_s = int(i), s
+        assert int(out["tokens"][0]) == best, trial
+        assert int(out["thresh_ties"][0]) == 0
+
+
+def test_keep_ties_equals_exact_k_when_the_cut_is_clean():
+    from vocab_wide_logit_gb300 import workloads as wl
+    inp = wl.config1()
+    c_bits = wl.bf16_bits(inp.c_logits)
+    u_bits = wl.bf16_bits(inp.u_logits)
+    a = oracle.sample_cells(inp.request_ids, c_bits, u_bits, inp.seq_lens, inp.C, inp.P, inp.V, inp.guidance,
+                            inp.temperature, inp.top_ratio, inp.seed, 0)
+    b = oracle.sample_cells(inp.request_ids, c_bits, u_bits, inp.seq_lens, inp.C, inp.P, inp.V, inp.guidance,
+                            inp.temperature, inp.top_ratio, inp.seed, 0, keep_ties=True)
+    clean = a["thresh_ties"] == 0
+    assert clean.mean() > 0.5
+    assert np.array_equal(a["tokens"][clean], b["tokens"][clean])
+    # where ties straddle the cut the kept set only grows: the exact-k winner's score cannot beat b's
+    assert np.all(b["top1"][~clean] >= a["top1"][~clean])

@@ -116,14 +116,20 @@ ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void
  *   iterations   device uint32 [B] or NULL. When given, request r's noise uses
  *                iterations[r] (< 2^24, else as an invalid ratio) and iteration
  *                is ignored.
- * With both NULL this is ds_sample. Per-request arrays must be 4-byte aligned.
- * Returns as ds_sample.
+ *   flags        0, or DS_FLAG_KEEP_TIES: the kept set becomes every id whose z
+ *                reaches the k-th largest z, so ids tied with the k-th are kept
+ *                too (the pages' "keep the ceil(0.1 V) largest" leaves ties at
+ *                the cut open; by default exactly k are kept, smallest ids first).
+ * With both arrays NULL and flags 0 this is ds_sample. Per-request arrays must
+ * be 4-byte aligned. Unknown flag bits: DS_ERR_INVALID_ARG. Returns as ds_sample.
  */
+#define DS_FLAG_KEEP_TIES 1u
 ds_status ds_sample_ex(const int32_t* request_ids, const void* c_logits, const void* u_logits,
                        const int32_t* seq_lens, int32_t B, int32_t C, int32_t P, int32_t V,
                        const float* guidance, const float* temperature, const float* top_ratios,
                        float top_ratio, uint64_t seed, const uint32_t* iterations, uint32_t iteration,
-                       int32_t* out_tokens, float* out_logprobs, uint32_t* d_status, void* stream);
+                       uint32_t flags, int32_t* out_tokens, float* out_logprobs, uint32_t* d_status,
+                       void* stream);
 
 /*
  * ds_greedy_lse -- per-row max, logsumexp and argmax of bf16 logits [n][V].

@@ -123,8 +123,8 @@ def test_reveal_argument_errors(lib):
 def test_sample_ex_argument_errors(lib):
     f = FAKE
 
-    def ex(ratios=None, ratio=0.1, iters=None, it=0, V=8):
-        return lib.ds_sample_ex(f, f, None, f, 1, 1, 1, V, f, f, ratios, ratio, 0, iters, it, f, f, None, None)
+    def ex(ratios=None, ratio=0.1, iters=None, it=0, V=8, flags=0):
+        return lib.ds_sample_ex(f, f, None, f, 1, 1, 1, V, f, f, ratios, ratio, 0, iters, it, flags, f, f, None, None)
 
     # the scalars are checked only when no per-request array replaces them
     assert ex(ratio=0.0) == _lib.DS_ERR_INVALID_ARG
@@ -132,4 +132,5 @@ def test_sample_ex_argument_errors(lib):
     assert ex(ratios=ctypes.c_void_p(0x100002), ratio=0.0) == _lib.DS_ERR_INVALID_ARG  # misaligned array
     assert ex(iters=ctypes.c_void_p(0x100001), it=1 << 24) == _lib.DS_ERR_INVALID_ARG
     assert ex(V=_lib.DS_MAX_VOCAB + 1) == _lib.DS_ERR_UNSUPPORTED
-    assert lib.ds_sample_ex(f, f, None, f, 1, 0, 1, 8, f, f, None, 0.1, 0, None, 0, f, f, None, None) == _lib.DS_OK
+    assert ex(flags=2) == _lib.DS_ERR_INVALID_ARG
+    assert lib.ds_sample_ex(f, f, None, f, 1, 0, 1, 8, f, f, None, 0.1, 0, None, 0, 1, f, f, None, None) == _lib.DS_OK

@@ -385,3 +385,26 @@ def test_per_request_invalid_ratio_is_reported_per_request():
     t = tok.cpu().numpy()
     assert (t[:, 4:] == -1).all() and (t[:, :4] >= 0).all()
     assert np.isnan(lp.cpu().numpy()[:, 4:]).all()
+
+
+@pytest.mark.parametrize("V,ratio", [(1025, 0.1), (4097, 0.05), (20000, 0.1), (20000, 0.6), (70001, 0.3)])
+def test_keep_ties_mode(V, ratio):
+    """DS_FLAG_KEEP_TIES: every id tied with the k-th largest z is kept. Unguided bf16 logits give
+    exact ties at the cut; every sample kernel (warp, streaming + fix-up, staged) is covered."""
+    dev = _dev()
+    seq = np.array([5, 9, 3], np.int32)
+    inp = wl.make_sample_inputs("ties%d" % V, 2, seq, V, [0.0, 0.0, 1.5], [0.9, 2.0, 0.7], 2.0, 1.0, ratio,
+                                seed=V + 7)
+    d = Dev(inp, dev)
+    tok = torch.full((inp.C, inp.P), -7, dtype=torch.int32, device=dev)
+    lp = torch.full((inp.C, inp.P), 7.0, dtype=torch.float32, device=dev)
+    pkg.ds_sample(d.rid, d.c, d.u, d.sl, d.g, d.tau, inp.top_ratio, inp.seed, 2, tok, lp, d_status=d.status,
+                  keep_ties=True)
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0
+    args = (inp.request_ids, wl.bf16_bits(inp.c_logits), wl.bf16_bits(inp.u_logits), inp.seq_lens, inp.C, inp.P,
+            inp.V, inp.guidance, inp.temperature, inp.top_ratio, inp.seed, 2)
+    ref = oracle.sample_cells(*args, keep_ties=True)
+    compare(inp, tok.cpu().numpy().reshape(-1), lp.cpu().numpy().reshape(-1), ref, label="ties V%d" % V)
+    # the inputs do put ties across the cut (the exact-k mode leaves some tied ids out)
+    assert (oracle.sample_cells(*args)["thresh_ties"] > 0).any()

@@ -22,6 +22,7 @@ DS_MAX_VOCAB = 262137
 
 EXPORTED = ("ds_sample", "ds_greedy_lse", "ds_status_string", "ds_top_k", "ds_merge_triples", "ds_log_softmax",
             "ds_reveal", "ds_sample_ex")
+DS_FLAG_KEEP_TIES = 1
 DS_DTYPE_F32 = 0
 DS_DTYPE_BF16 = 1
 
@@ -58,7 +59,8 @@ def load(path: str = LIB_PATH):
     L.ds_log_softmax.restype = ctypes.c_int
     L.ds_reveal.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
     L.ds_reveal.restype = ctypes.c_int
-    L.ds_sample_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, f32, u64, vp, u32, vp, vp, vp, vp]
+    L.ds_sample_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, f32, u64, vp, u32, u32, vp, vp, vp,
+                               vp]
     L.ds_sample_ex.restype = ctypes.c_int
     _lib = L
     return L
@@ -85,7 +87,7 @@ def _stream(stream):
 
 def ds_sample(request_ids, c_logits, u_logits, seq_lens, guidance, temperature, top_ratio, seed,
               iteration, out_tokens, out_logprobs, d_status=None, B=None, C=None, P=None, V=None,
-              stream=None, check=True, top_ratios=None, iterations=None):
+              stream=None, check=True, top_ratios=None, iterations=None, keep_ties=False):
     """Call ds_sample (ds_sample_ex when per-request top_ratios / iterations are given) on device
     tensors. Shapes: c_logits [C, P, V] bf16, u_logits [C, P_u, V] bf16 or None,
     request_ids/seq_lens int32 [B], guidance/temperature float32 [B], top_ratios float32 [B] or
@@ -95,7 +97,7 @@ def ds_sample(request_ids, c_logits, u_logits, seq_lens, guidance, temperature, 
         C, P, V = c_logits.shape
     if B is None:
         B = seq_lens.shape[0]
-    if top_ratios is None and iterations is None:
+    if top_ratios is None and iterations is None and not keep_ties:
         rc = load().ds_sample(_ptr(request_ids), _ptr(c_logits), _ptr(u_logits), _ptr(seq_lens), int(B),
                               int(C), int(P), int(V), _ptr(guidance), _ptr(temperature), float(top_ratio),
                               int(seed) & (2 ** 64 - 1), int(iteration), _ptr(out_tokens), _ptr(out_logprobs),
@@ -105,7 +107,8 @@ def ds_sample(request_ids, c_logits, u_logits, seq_lens, guidance, temperature, 
         rc = load().ds_sample_ex(_ptr(request_ids), _ptr(c_logits), _ptr(u_logits), _ptr(seq_lens), int(B),
                                  int(C), int(P), int(V), _ptr(guidance), _ptr(temperature), _ptr(top_ratios),
                                  float(top_ratio), int(seed) & (2 ** 64 - 1), _ptr(iterations), int(iteration),
-                                 _ptr(out_tokens), _ptr(out_logprobs), _ptr(d_status), _stream(stream))
+                                 DS_FLAG_KEEP_TIES if keep_ties else 0, _ptr(out_tokens), _ptr(out_logprobs),
+                                 _ptr(d_status), _stream(stream))
         name = "ds_sample_ex"
     if check and rc != DS_OK:
         raise DsError(name, rc)

@@ -5,7 +5,8 @@ from . import _lib
 
 
 def sample(request_ids, c_logits, u_logits, seq_lens, guidance, temperature, top_ratio, seed, iteration,
-           out_tokens=None, out_logprobs=None, d_status=None, stream=None, top_ratios=None, iterations=None):
+           out_tokens=None, out_logprobs=None, d_status=None, stream=None, top_ratios=None, iterations=None,
+           keep_ties=False):
     """Sample every cell of c_logits [C, P, V] (bf16, cuda). Returns (tokens int32 [C, P],
     logprobs float32 [C, P]). top_ratios / iterations: optional per-request device arrays [B]."""
     C, P, V = c_logits.shape
@@ -16,7 +17,7 @@ def sample(request_ids, c_logits, u_logits, seq_lens, guidance, temperature, top
         out_logprobs = torch.empty((C, P), dtype=torch.float32, device=dev)
     _lib.ds_sample(request_ids, c_logits, u_logits, seq_lens, guidance, temperature, top_ratio, seed,
                    iteration, out_tokens, out_logprobs, d_status=d_status, stream=stream, top_ratios=top_ratios,
-                   iterations=iterations)
+                   iterations=iterations, keep_ties=keep_ties)
     return out_tokens, out_logprobs
 
 

@@ -70,8 +70,10 @@ ds_status ds_sample_ex(const int32_t* request_ids, const void* c_logits, const v
                        const int32_t* seq_lens, int32_t B, int32_t C, int32_t P, int32_t V,
                        const float* guidance, const float* temperature, const float* top_ratios,
                        float top_ratio, uint64_t seed, const uint32_t* iterations, uint32_t iteration,
-                       int32_t* out_tokens, float* out_logprobs, uint32_t* d_status, void* stream) {
+                       uint32_t flags, int32_t* out_tokens, float* out_logprobs, uint32_t* d_status,
+                       void* stream) {
   if (B < 0 || C < 0 || P < 0 || V < 1) return DS_ERR_INVALID_ARG;
+  if ((flags & ~(uint32_t)DS_FLAG_KEEP_TIES) != 0u) return DS_ERR_INVALID_ARG;
   if (C > DS_MAX_ROWS) return DS_ERR_INVALID_ARG;
   if (!iterations && iteration > DS_MAX_ITERATION) return DS_ERR_INVALID_ARG;
   if (!top_ratios && !(top_ratio > 0.0f && top_ratio <= 1.0f)) return DS_ERR_INVALID_ARG;
@@ -102,6 +104,7 @@ ds_status ds_sample_ex(const int32_t* request_ids, const void* c_logits, const v
   a.V = V;
   a.ratios = top_ratios;
   a.iters = iterations;
+  a.keep_ties = (flags & DS_FLAG_KEEP_TIES) ? 1u : 0u;
   // scalar kept count and threshold guesses (used when no per-request ratios are given)
   a.k = top_ratios ? 1 : ds_top_k(top_ratio, V);
   // Threshold guesses: aim the candidate count a little above k so that the
@@ -145,7 +148,7 @@ ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void
                     uint64_t seed, uint32_t iteration, int32_t* out_tokens, float* out_logprobs,
                     uint32_t* d_status, void* stream) {
   return ds_sample_ex(request_ids, c_logits, u_logits, seq_lens, B, C, P, V, guidance, temperature, nullptr,
-                      top_ratio, seed, nullptr, iteration, out_tokens, out_logprobs, d_status, stream);
+                      top_ratio, seed, nullptr, iteration, 0u, out_tokens, out_logprobs, d_status, stream);
 }
 
 ds_status ds_greedy_lse(const void* logits, int32_t n, int32_t V, float* out_max, float* out_lse,

@@ -34,7 +34,14 @@ struct SampleArgs {
   uint32_t rk0[10], rk1[10];  // Philox round keys (key + r * Weyl constants), computed on the host
   const float* ratios;        // per-request top ratio [B] (device) or null: k, q_lo, q_hi above
   const uint32_t* iters;      // per-request iteration [B] (device) or null: iter_hi above
+  uint32_t keep_ties;         // 1: the kept set is every z reaching the k-th largest z
 };
+
+// Key used for kept-set membership: the full (z desc, id asc) composite key, or
+// with keep_ties only its z part (every id tied with the k-th z is kept).
+__device__ __forceinline__ unsigned long long member_key(unsigned long long key, uint32_t keep_ties) {
+  return keep_ties ? (key | 0xffffffffull) : key;
+}
 
 // ---------------------------------------------------------------- loads
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {

@@ -608,7 +608,7 @@ __global__ void __launch_bounds__(NT, 2) k_sample_cluster(const SampleArgs a, in
         for (int i = tid; i < nL; i += NT) {
           const int l = idxs[i];
           const float zi = zs[l];
-          rr += (zi > zw || (zi == zw && id_base + l < idw)) ? 1 : 0;
+          rr += (zi > zw || (!a.keep_ties && zi == zw && id_base + l < idw)) ? 1 : 0;
         }
         if (cluster_sum<NT>(cl, xs, red, rr, parity, cs) >= k) exact = true;
       }
@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(NT, 2) k_sample_cluster(const SampleArgs a, in
         const int l = idxs[i];
         const float zi = zs[l];
         const int id = id_base + l;
-        if (rank_key(zi, id) >= kth) {
+        if (member_key(rank_key(zi, id), a.keep_ties) >= member_key(kth, a.keep_ties)) {
           const uint32_t x = noise_word((uint32_t)id, t32, cur.rid, ctr3, a.rk0, a.rk1);
           const float scr = __fmaf_rn(tau, gumbel_accurate(x), zi);
           if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {

@@ -147,7 +147,7 @@ __device__ __forceinline__ float2 race_exact(const SampleArgs& a, Get get, int n
     float2 v;
     if (!get(it, v)) continue;
     const int id = __float_as_int(v.y);
-    if (rank_key(v.x, id) >= kth) {
+    if (member_key(rank_key(v.x, id), a.keep_ties) >= member_key(kth, a.keep_ties)) {
       const uint32_t x = noise_word((uint32_t)id, t32, rid, ctr3, a.rk0, a.rk1);
       const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
       if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
@@ -296,10 +296,10 @@ __device__ __forceinline__ float2 race_dense(const SampleArgs& a, const float2* 
         int c = 0;
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          c += (keep[u].x > w.x || (keep[u].x == w.x && __float_as_int(keep[u].y) < idw)) ? 1 : 0;
+          c += (keep[u].x > w.x || (!a.keep_ties && keep[u].x == w.x && __float_as_int(keep[u].y) < idw)) ? 1 : 0;
         rr = warp_sum_i(c);
       } else {
-        rr = rank_of(get, n_it, w.x, __float_as_int(w.y));
+        rr = rank_of(get, n_it, w.x, a.keep_ties ? INT_MIN : __float_as_int(w.y));
       }
       if (rr >= k) exact = true;
     }
@@ -333,7 +333,7 @@ __device__ __forceinline__ float2 race_generic(const SampleArgs& a, WarpSmem<NCH
   if (!exact) {
     const float thr = S - (fabsf(S) + 1.f) * 0x1p-20f;
     w = race_resolve(a, get, items.n_it, thr, tau, t32, rid, ctr3);
-    if (ctot > k && rank_of(get, items.n_it, w.x, __float_as_int(w.y)) >= k) exact = true;
+    if (ctot > k && rank_of(get, items.n_it, w.x, a.keep_ties ? INT_MIN : __float_as_int(w.y)) >= k) exact = true;
   }
   if (exact) {
     const unsigned long long kth = (ctot > k) ? kth_key(get, items.n_it, k, lane, sm.hist) : 0ull;

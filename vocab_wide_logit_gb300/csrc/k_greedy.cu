@@ -8,9 +8,13 @@
 // memory instead of an all-gather between GPUs.
 //
 // One streaming pass: each thread walks 16-byte chunks keeping an online (max,
-// sum of exp(x - max), smallest argmax), rescaled once per batch of chunks, so
-// each logit costs one exp. Interior chunks run in unchecked batches; only the
-// row's first and last chunk go through the masked path.
+// sum of exp(x - max), first chunk holding the max), rescaled once per batch
+// of chunks, so each logit costs one exp. A thread visits its chunks in
+// increasing order, so the first chunk to reach a new max holds the thread's
+// smallest argmax; merges keep the smaller chunk on equal maxima, and one
+// thread re-reads the winning chunk (16 bytes) to name the element. Interior
+// chunks run in unchecked batches; only the row's first and last chunk go
+// through the masked path.
 #include <climits>
 #include <cooperative_groups.h>
 #include <type_traits>
@@ -25,7 +29,7 @@ namespace ds {
 struct Triple {
   float m;  // max
   float s;  // sum of exp(x - m)
-  int a;    // smallest id attaining m
+  int a;    // first 16-byte chunk attaining m (chunks are disjoint and in id order)
 };
 
 __device__ __forceinline__ Triple merge(const Triple& p, const Triple& q) {
@@ -116,23 +120,20 @@ __global__ void __launch_bounds__(NT, 2) k_greedy_lse(const uint16_t* __restrict
 #pragma unroll
         for (int i = 0; i < 4; ++i) bm = max3g(bm, f[u][i].x, f[u][i].y);
       }
-      if (bm >= t.m && bm > -kInf) {
-        // new (or equal) running max: rescale the sum; keep the smallest id attaining it
-        if (bm > t.m) {
-          t.s = (t.m == -kInf) ? 0.f : t.s * ex2_approx((t.m - bm) * kLog2e);
-          t.m = bm;
-          t.a = INT_MAX;
-        }
+      if (bm > t.m) {
+        // a new running max: rescale the sum; the first chunk of this batch
+        // holding it (an equal max later in the walk has larger ids)
+        t.s = (t.m == -kInf) ? 0.f : t.s * ex2_approx((t.m - bm) * kLog2e);
+        t.m = bm;
         int a = INT_MAX;
 #pragma unroll
-        for (int u = NCHK - 1; u >= 0; --u)
-#pragma unroll
-          for (int i = 3; i >= 0; --i) {
-            const int id = 8 * (q0 + u * NT) - dc + 2 * i;
-            if (f[u][i].y == bm) a = id + 1;
-            if (f[u][i].x == bm) a = id;
-          }
-        t.a = min(t.a, a);
+        for (int u = NCHK - 1; u >= 0; --u) {
+          float c = max3g(f[u][0].x, f[u][0].y, f[u][1].x);
+          c = max3g(c, f[u][1].y, f[u][2].x);
+          c = max3g(c, f[u][2].y, f[u][3].x);
+          if (fmaxf(c, f[u][3].y) == bm) a = q0 + u * NT;
+        }
+        t.a = a;
       }
       if (t.m != -kInf) {
         const float2 nml = make_float2(-t.m * kLog2e, -t.m * kLog2e);
@@ -190,9 +191,23 @@ __global__ void __launch_bounds__(NT, 2) k_greedy_lse(const uint16_t* __restrict
         const Triple* peer = cluster.map_shared_rank(&cta_part, j);
         r = merge(r, *peer);
       }
+      // the element: the first id of the winning chunk whose logit equals the max
+      int am = 0;
+      if (r.a != INT_MAX) {
+        const uint4 v = __ldg(base + r.a);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        am = INT_MAX;
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+          const float xi = (i & 1) ? bf_hi(w[i >> 1]) : bf_lo(w[i >> 1]);
+          const int id = 8 * r.a - dc + i;
+          if (id >= 0 && id < V && xi == r.m) am = id;
+        }
+        if (am == INT_MAX) am = 0;  // not reached: the chunk holds the max
+      }
       out_max[row] = r.m;
       out_lse[row] = (r.m == -kInf) ? -kInf : r.m + logf(r.s);
-      out_argmax[row] = (r.a == INT_MAX) ? 0 : r.a;
+      out_argmax[row] = am;
     }
     cluster.sync();  // peers' partials stay alive until rank 0 has read them
   }

@@ -277,9 +277,28 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
       return make_uint4(w[0], w[1], w[2], w[3]);
     };
 
+    // first id of chunk q whose z equals zt (INT_MAX if none): z formed from the
+    // two logits exactly as in the pass, ids outside the row masked
+    auto chunk_first_id = [&](int q, float zt) -> int {
+      const uint4 vc = __ldg(cb + q);
+      const uint4 vu = guided ? load_u(q) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w};
+      const uint32_t wu[4] = {vu.x, vu.y, vu.z, vu.w};
+      int id = INT_MAX;
+#pragma unroll
+      for (int i = 7; i >= 0; --i) {
+        const float ci = (i & 1) ? bf_hi(wc[i >> 1]) : bf_lo(wc[i >> 1]);
+        const float ui = (i & 1) ? bf_hi(wu[i >> 1]) : bf_lo(wu[i >> 1]);
+        const float zi = guided ? __fmaf_rn(g, __fmaf_rn(ui, -1.f, ci), ci) : ci;
+        const int e = 8 * q - dc + i;
+        if (e >= 0 && e < V && zi == zt) id = e;
+      }
+      return id;
+    };
+
     // ---- race state (queue lengths and flags are warp-uniform)
     float m = -kInf, s = 0.f;
-    int am = INT_MAX;
+    int am = INT_MAX;  // first chunk holding m
     float SAl = -kInf;           // best lower-bound score this warp knows of
     int ns = 0, ne = 0, nl = 0;  // staged chunks, queued elements, live elements
     int E = 0;                   // elements this warp sent to the noise stage
@@ -439,25 +458,17 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
           bm = fmaxf(bm, cmx[uu]);
         }
         if (MODE != 2) {
-          if (bm >= m && bm > -kInf) {
-            // a new (or equal) running max: rescale the sum; keep the smallest id
-            // attaining it (chunks are not visited in id order, so take the min)
-            if (bm > m) {
-              s = (m == -kInf) ? 0.f : s * ex2_approx((m - bm) * kLog2e);
-              m = bm;
-              am = INT_MAX;
-            }
+          if (bm > m) {
+            // a new running max: rescale the sum; remember the first chunk of the
+            // batch holding it (a thread walks its chunks in increasing order, so
+            // an equal max met later has larger ids)
+            s = (m == -kInf) ? 0.f : s * ex2_approx((m - bm) * kLog2e);
+            m = bm;
             int aa = INT_MAX;
 #pragma unroll
-            for (int uu = NCHK - 1; uu >= 0; --uu) {
-#pragma unroll
-              for (int i = 3; i >= 0; --i) {
-                const int id = 8 * (q0 + uu * NT) - dc + 2 * i;
-                if (z[uu][i].y == bm) aa = id + 1;
-                if (z[uu][i].x == bm) aa = id;
-              }
-            }
-            am = min(am, aa);
+            for (int uu = NCHK - 1; uu >= 0; --uu)
+              if (cmx[uu] == bm) aa = q0 + uu * NT;
+            am = aa;
           }
           if (m != -kInf) {
             const float2 nml = make_float2(-m * kLog2e, -m * kLog2e);
@@ -537,7 +548,8 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
             bi = i2;
           }
         }
-        if (bz > -kInf) {
+        if (bz > -kInf) bi = chunk_first_id(bi, bz);  // the anchor element of the first chunk holding bz
+        if (bz > -kInf && bi != INT_MAX) {
           const uint32_t x = noise_word((uint32_t)bi, t32, cur.rid, ctr3, a.rk0, a.rk1);
           const float lo = __fmaf_rn(tau, gumbel_bounds(x).x, bz);
           if (wid == 0) publish(lo);
@@ -619,7 +631,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
       lse = (m == -kInf) ? -kInf : m + logf(R.f[1]);
       if (m == -kInf || !sampled) {  // all -inf (token 0, logprob NaN) or temperature 0 (the argmax)
         if (rank == 0 && tid == 0) {
-          a.out_tokens[cell] = (m == -kInf) ? 0 : am;
+          a.out_tokens[cell] = (m == -kInf) ? 0 : chunk_first_id(am, m);
           a.out_logprobs[cell] = (m == -kInf) ? __int_as_float(0x7fc00000) : m - lse;
         }
         __syncthreads();

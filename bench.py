@@ -331,6 +331,19 @@ def roofline(bytes_per_step, ms, workload, kernel=None):
             "traffic": committed_traffic(workload), "algorithmic_bytes_per_launch": bytes_per_step}
 
 
+def metric_name(is_greedy):
+    return ("greedy rows/s (max/LSE/argmax, V=248320)" if is_greedy else
+            "sampled positions/s (fused CFG + top-ratio + Gumbel, HBM roofline fraction alongside)")
+
+
+def run_config(w, is_greedy, world):
+    """The workload description both arms report (the reference arm times the same workload)."""
+    return {"workload": w.name, "units_per_gpu_step": w.n if is_greedy else w.cells,
+            "bytes_per_gpu_step": w.algorithmic_bytes(),
+            "l2": "4 rotating input buffers, 508 MB total > L2" if is_greedy else "inputs larger than L2 (no flush)",
+            "parallelism": "dp%d (independent cells per rank)" % world}
+
+
 # ------------------------------------------------------------------------------------- arms
 def run_ours(args):
     rank, world, local = dist_env()
@@ -354,16 +367,11 @@ def run_ours(args):
     value = units / (ms / 1e3)
     unit = "rows/s" if is_greedy else "sampled positions/s"
     line = {
-        "metric": "greedy rows/s (max/LSE/argmax, V=248320)" if is_greedy else
-        "sampled positions/s (fused CFG + top-ratio + Gumbel, HBM roofline fraction alongside)",
+        "metric": metric_name(is_greedy),
         "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded, bf16 inputs)",
-        "config": {"workload": w.name, "units_per_gpu_step": runner.units,
-                   "bytes_per_gpu_step": runner.bytes_per_step,
-                   "l2": "inputs larger than L2 (no flush)" if not is_greedy else
-                   "4 rotating input buffers, 508 MB total > L2",
-                   "parallelism": "dp%d (independent cells per rank)" % world},
+        "config": run_config(w, is_greedy, world),
         "roofline": roofline(runner.bytes_per_step, ms, wname, dominant_kernel(w)),
         "gpu_launches": args.steps * launches_per_step(w),
         "clocks": clocks,
@@ -425,12 +433,11 @@ def run_reference(args):
         if i >= args.warmup:
             rates.append(r)
     value = statistics.median(rates)
-    line = {"impl": "reference", "metric": "sampled positions/s (fused CFG + top-ratio + Gumbel)"
-            if not is_greedy else "greedy rows/s (max/LSE/argmax, V=248320)",
+    line = {"impl": "reference", "metric": metric_name(is_greedy),
             "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded, bf16 inputs)",
-            "config": {"workload": w.name, "parallelism": "single host thread"},
+            "config": run_config(w, is_greedy, world),
             "cpu_baseline": {"value": round(value, 2), "unit": unit, "cores": 1, "kind": "oracle",
                              "sample": sample + " per step", "host_cpus": os.cpu_count()},
             "e2e": {"value": round(value, 2), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -408,3 +408,38 @@ def test_keep_ties_mode(V, ratio):
     compare(inp, tok.cpu().numpy().reshape(-1), lp.cpu().numpy().reshape(-1), ref, label="ties V%d" % V)
     # the inputs do put ties across the cut (the exact-k mode leaves some tied ids out)
     assert (oracle.sample_cells(*args)["thresh_ties"] > 0).any()
+
+
+# ------------------------------------------------------------------------------------------ limits
+@pytest.mark.parametrize("ratio", [0.01, 0.5])
+def test_largest_vocabulary(ratio):
+    """V = DS_MAX_VOCAB on both large-vocabulary paths: the streaming pass with its fix-up (small
+    k) and the staged kernel alone with 16-CTA clusters (large k)."""
+    dev = _dev()
+    V = pkg.DS_MAX_VOCAB
+    inp = wl.make_sample_inputs("vmax", C=1, seq_lens=[2, 3], V=V, guidance=[1.5, 0.0], temperature=[0.7, 1.2],
+                                sigma_c=4.0, sigma_u=2.0, top_ratio=ratio, seed=21)
+    d = Dev(inp, dev)
+    tok, lp = d.run(3, 7)
+    compare(inp, tok, lp, oracle_cells(inp, 3, 7), label="V=%d ratio %g" % (V, ratio))
+    assert int(d.status.item()) == 0
+
+
+def test_most_rows_last_iteration_and_many_requests():
+    """C = DS_MAX_ROWS rows, iteration 2^24 - 1 (both key the noise), and 3000 requests, so the
+    position -> request walk crosses many warp-wide scans."""
+    dev = _dev()
+    rng = np.random.Generator(np.random.PCG64(77))
+    B = 3000
+    seq = rng.integers(0, 3, size=B).astype(np.int32)
+    seq[0] = 1
+    g = np.where(rng.random(B) < 0.5, 2.0, 0.0).astype(np.float32)
+    tau = np.where(rng.random(B) < 0.2, 0.0, 0.9).astype(np.float32)
+    inp = wl.make_sample_inputs("limits", C=256, seq_lens=seq, V=33, guidance=g, temperature=tau, sigma_c=2.0,
+                                sigma_u=1.0, top_ratio=0.3, seed=31)
+    d = Dev(inp, dev)
+    it = (1 << 24) - 1
+    tok, lp = d.run(2 ** 63 + 5, it)
+    cells = np.sort(rng.choice(inp.C * inp.P, size=4000, replace=False))
+    compare(inp, tok, lp, oracle_cells(inp, 2 ** 63 + 5, it, cells), cells, label="limits")
+    assert int(d.status.item()) == 0

@@ -32,13 +32,30 @@ namespace ds {
 
 constexpr int kDenseCap = 256;  // candidates gathered into one balanced list
 
+// The candidate columns are dead once the balanced list is built. From then on
+// the same bytes hold the race's upper scores and histogram and the next cell's
+// logits, which cp.async copies in while the race runs.
 template <int NCH>
 struct WarpSmem {
-  float2 col[NCH * 8 + 1][32];  // per-lane candidate columns: (z, id as int bits)
-  float2 dense[kDenseCap];      // balanced candidate list
-  float hs[kDenseCap];          // upper-bound score of each dense candidate
-  int hist[256];                // radix histogram of the exact fallback; overlap list of the race
+  union {
+    float2 col[NCH * 8 + 1][32];  // per-lane candidate columns: (z, id as int bits)
+    struct {
+      float hs[kDenseCap];        // upper-bound score of each dense candidate
+      int hist[256];              // radix histogram of the exact fallback; overlap list of the race
+      uint4 rawc[NCH][32];        // the next cell's c chunks (chunk lane + 32 j)
+      uint4 rawu[NCH][32];        // and its u chunks
+    } r;
+  };
+  float2 dense[kDenseCap];  // balanced candidate list (the histogram while the columns race)
 };
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
@@ -336,20 +353,24 @@ __device__ __forceinline__ float2 race_generic(const SampleArgs& a, WarpSmem<NCH
     if (ctot > k && rank_of(get, items.n_it, w.x, a.keep_ties ? INT_MIN : __float_as_int(w.y)) >= k) exact = true;
   }
   if (exact) {
-    const unsigned long long kth = (ctot > k) ? kth_key(get, items.n_it, k, lane, sm.hist) : 0ull;
+    const unsigned long long kth =
+        (ctot > k) ? kth_key(get, items.n_it, k, lane, reinterpret_cast<int*>(sm.dense)) : 0ull;
     w = race_exact(a, get, items.n_it, kth, tau, t32, rid, ctr3);
   }
   return w;
 }
 
+// Starts the copies of a cell's logits into this warp's shared buffers: each
+// lane copies its own chunks (lane + 32 j), so it later reads only what it
+// copied. The scalar head or tail element goes to registers.
 template <int NCH>
-__device__ __forceinline__ void load_cell(const CellGeo& G, int lane, uint4 (&rc)[NCH], uint4 (&ru)[NCH],
-                                          uint32_t& sc, uint32_t& su) {
+__device__ __forceinline__ void prefetch_cell(const CellGeo& G, int lane, WarpSmem<NCH>& sm, uint32_t& sc,
+                                              uint32_t& su) {
   const uint4* cb = reinterpret_cast<const uint4*>(G.crow + G.h);
 #pragma unroll
   for (int j = 0; j < NCH; ++j) {
     const int q = lane + 32 * j;
-    rc[j] = (q < G.nfc) ? ld_stream16(cb + q) : make_uint4(0u, 0u, 0u, 0u);
+    cp_async16(&sm.r.rawc[j][lane], (q < G.nfc) ? cb + q : cb, (q < G.nfc) ? 16u : 0u);
   }
   sc = (lane < G.ns) ? (uint32_t)__ldg(G.crow + G.sid) : 0u;
   su = 0u;
@@ -359,7 +380,7 @@ __device__ __forceinline__ void load_cell(const CellGeo& G, int lane, uint4 (&rc
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
         const int q = lane + 32 * j;
-        ru[j] = (q < G.nfc) ? ld_stream16(ub + q) : make_uint4(0u, 0u, 0u, 0u);
+        cp_async16(&sm.r.rawu[j][lane], (q < G.nfc) ? ub + q : ub, (q < G.nfc) ? 16u : 0u);
       }
     } else {
       // u row aligned differently from the c row: gather element by element.
@@ -373,21 +394,18 @@ __device__ __forceinline__ void load_cell(const CellGeo& G, int lane, uint4 (&rc
           for (int hh = 0; hh < 4; ++hh)
             w[hh] = (uint32_t)__ldg(src + 2 * hh) | ((uint32_t)__ldg(src + 2 * hh + 1) << 16);
         }
-        ru[j] = make_uint4(w[0], w[1], w[2], w[3]);
+        sm.r.rawu[j][lane] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     su = (lane < G.ns) ? (uint32_t)__ldg(G.urow + G.sid) : 0u;
   }
+  cp_async_commit();
 }
 
-// Occupancy and prefetch placement (measured on GB300 at V = 1025): 3 CTAs of 4
-// warps per SM with the next cell's loads issued before the race is fastest;
-// a 4-CTA register budget spills.
+// Occupancy: with the next cell's logits in shared memory rather than
+// registers, 4 CTAs of 4 warps fit per SM.
 #ifndef DS_WARP_MINB
-#define DS_WARP_MINB 3
-#endif
-#ifndef DS_PREFETCH_EARLY
-#define DS_PREFETCH_EARLY 1
+#define DS_WARP_MINB 4
 #endif
 
 template <int NCH>
@@ -468,18 +486,18 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
     return G;
   };
 
-  uint4 rc[NCH], ru[NCH];
   uint32_t sc = 0u, su = 0u;
   CellGeo nxt = next_geo(cbeg);
-  if (nxt.err == 0u) load_cell<NCH>(nxt, lane, rc, ru, sc, su);
+  if (nxt.err == 0u) prefetch_cell<NCH>(nxt, lane, sm, sc, su);
 
   for (long long cell = cbeg; cell < cend; ++cell) {
+    cp_async_wait_all();  // this lane's chunks of the cell have landed
     const CellGeo G = nxt;
     const bool has_next = cell + 1 < cend;
     auto prefetch_next = [&]() {
       if (has_next) {
         nxt = next_geo(cell + 1);
-        if (nxt.err == 0u) load_cell<NCH>(nxt, lane, rc, ru, sc, su);
+        if (nxt.err == 0u) prefetch_cell<NCH>(nxt, lane, sm, sc, su);
       }
     };
     if (G.err != 0u) {
@@ -503,8 +521,10 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
     float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
-      const uint32_t wc[4] = {rc[j].x, rc[j].y, rc[j].z, rc[j].w};
-      const uint32_t wu[4] = {ru[j].x, ru[j].y, ru[j].z, ru[j].w};
+      const uint4 vc = sm.r.rawc[j][lane];
+      const uint4 vu = guided ? sm.r.rawu[j][lane] : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w};
+      const uint32_t wu[4] = {vu.x, vu.y, vu.z, vu.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 cp = make_float2(bf_lo(wc[i]), bf_hi(wc[i]));
@@ -532,6 +552,7 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
         s2 = __ffma2_rn(z[j][3], z[j][3], s2);
       }
     }
+    __syncwarp();  // every lane has read its chunks: the columns may overwrite them
     float zs1;
     {
       const float cf = __uint_as_float(sc << 16);
@@ -646,10 +667,6 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
       cnt = (int)((ca - col0) >> 8);
       ctot = warp_sum_i(cnt);
     }
-#if DS_PREFETCH_EARLY
-    // z is dead from here on: start loading the next cell while this one races
-    prefetch_next();
-#endif
     const float lse = m + logf(warp_sum(ssum));
     __syncwarp();
     Items items;
@@ -658,6 +675,8 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
       const int base = warp_excl_scan(cnt, lane);
       for (int j = 0; j < cnt; ++j) sm.dense[base + j] = sm.col[j][lane];
       __syncwarp();
+      // the columns are dead: the next cell's logits load while this one races
+      prefetch_next();
       items.n = ctot;
       items.n_it = (ctot + 31) >> 5;
     } else {
@@ -671,14 +690,12 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
     const uint32_t rid = G.rid;
     float2 w;
     if (items.dense) {
-      w = race_dense(a, sm.dense, sm.hs, ctot, k, tau, t32, rid, ctr3, lane, sm.hist);
+      w = race_dense(a, sm.dense, sm.r.hs, ctot, k, tau, t32, rid, ctr3, lane, sm.r.hist);
     } else {
       w = race_generic<NCH>(a, sm, items, ctot, k, tau, t32, rid, ctr3, lane);
+      __syncwarp();
+      prefetch_next();
     }
-
-#if !DS_PREFETCH_EARLY
-    prefetch_next();
-#endif
     // ---- step 5: output
     if (lane == 0) {
       a.out_tokens[cell] = __float_as_int(w.y);

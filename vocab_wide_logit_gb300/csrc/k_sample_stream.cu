@@ -157,8 +157,17 @@ __device__ __forceinline__ SRec cluster_combine(cg::cluster_group& cl, SXchg& xs
 
 constexpr int kStreamNT = 256;
 constexpr int kStreamUnroll = 2;
+// A noise word whose lower bound is at least this gets G evaluated exactly
+// when it is drawn. The table's buckets are uniform in the word, so they widen
+// without limit as U -> 1 (the top one spans G in [7.6, 17.3]); at large V
+// the winner usually lies there, and exact values keep SA tight and the final
+// bounds apart. About 0.25% of the draws take this branch.
+constexpr float kExactGFrom = 6.0f;
 
-template <int NT, int UNROLL>
+// ALIGNED: every c and u row starts on a 16-byte boundary (V a multiple of 8,
+// both buffers 16-byte aligned), so chunks never straddle rows and u never
+// needs the element-wise gather.
+template <int NT, int UNROLL, bool ALIGNED>
 __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
   pdl_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -250,7 +259,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
     const uint16_t* crow = a.c + cell * (long long)V;
     const uintptr_t ca = reinterpret_cast<uintptr_t>(crow);
     const uint4* cb = reinterpret_cast<const uint4*>(ca & ~(uintptr_t)15);
-    const int dc = (int)((ca & 15) >> 1);
+    const int dc = ALIGNED ? 0 : (int)((ca & 15) >> 1);
     const int nq = (dc + V + 7) >> 3;
     const int q_lo = (int)((long long)rank * nq / cs);
     const int q_hi = (int)((long long)(rank + 1) * nq / cs);
@@ -261,7 +270,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
       urow = a.u + ((long long)c * P_u + cur.off_u + t) * (long long)V;
       const uintptr_t ua = reinterpret_cast<uintptr_t>(urow);
       ub = reinterpret_cast<const uint4*>(ua & ~(uintptr_t)15);
-      u_aligned = (ua & 15) == (ca & 15);
+      u_aligned = ALIGNED || (ua & 15) == (ca & 15);
     }
     auto load_u = [&](int q) -> uint4 {
       if (u_aligned) return ld_stream16(ub + q);
@@ -341,7 +350,11 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
       if (on) {
         v = W.eq[i];
         const uint32_t x = noise_word(__float_as_uint(v.y), t32, cur.rid, ctr3, a.rk0, a.rk1);
-        const float2 gb = gumbel_bounds(x);
+        float2 gb = gumbel_bounds(x);
+        if (gb.x >= kExactGFrom) {
+          const float ge = gumbel_accurate(x);
+          gb = make_float2(ge, ge);
+        }
         lo = __fmaf_rn(tau, gb.x, v.x);
         hi = __fmaf_rn(tau, gb.y, v.x);
       }
@@ -693,7 +706,10 @@ cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
   // up to 4 CTAs per row: enough logits per thread to amortise the per-cell rounds
   int cs = 1;
   while (cs < 4 && nq_max / cs > 2 * kStreamNT * kStreamUnroll) cs *= 2;
-  auto kern = k_sample_stream<kStreamNT, kStreamUnroll>;
+  const bool aligned = (a.V % 8) == 0 && (reinterpret_cast<uintptr_t>(a.c) & 15) == 0 &&
+                       (reinterpret_cast<uintptr_t>(a.u) & 15) == 0;
+  auto kern = aligned ? k_sample_stream<kStreamNT, kStreamUnroll, true>
+                      : k_sample_stream<kStreamNT, kStreamUnroll, false>;
   const size_t smem = sizeof(WarpArea) * (kStreamNT / 32);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -5,6 +5,8 @@ T ~ U{100..400} positions (P = 15510, 124080 cells), V = 1025, bf16 c and u,
 guidance 2, temperature 0.9, top ratio 0.1, seed 2. One step = one ds_sample call
 over the whole batch (iteration counter = step index mod 32). Inputs are 510 MB,
 far above the 129 MB L2, so no flush is needed between steps.
+`ms_per_call` adds the median and minimum of 64 single calls, each between its own
+pair of events, timed after the contract's region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload cfg3|cfg5|cfg4|cfg1|cfg2] [--no-extra]
@@ -237,6 +239,21 @@ def time_steps(runner, steps, warmup, world, timer=None, device="cuda"):
     return ms / steps
 
 
+def per_call_ms(runner, calls, first_step):
+    """Median and minimum device time of single calls, one event pair per call, taken after
+    (and apart from) the timed region so that its events do not perturb the contract's number."""
+    st = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(ev):
+        a.record(st)
+        runner.step(first_step + i)
+        b.record(st)
+    torch.cuda.synchronize()
+    t = sorted(a.elapsed_time(b) for a, b in ev)
+    return {"median": round(statistics.median(t), 5), "min": round(t[0], 5), "calls": calls}
+
+
 def launches_per_step(w):
     """Kernels one ds_sample / ds_greedy_lse call launches (mirrors the library's dispatch:
     one warp-per-cell kernel up to V = 2055; the streaming kernel plus its fix-up pass when
@@ -379,6 +396,7 @@ def run_ours(args):
     if rank == 0 and not is_greedy:
         line["logit_elements_per_s"] = round(value * w.V, 1)
     if rank == 0:
+        line["ms_per_call"] = per_call_ms(runner, 64, args.warmup + args.steps)
         # end to end through the public API, from pinned host memory
         if not is_greedy:
             ev, hb, db = e2e_rate(w, dev, max(3, min(args.steps, 10)))
@@ -403,6 +421,7 @@ def run_ours(args):
                 runner = GreedyRunner(ow, dev) if other == "cfg4" else SampleRunner(ow, dev)
                 oms = time_steps(runner, max(10, min(args.steps, 1500)), args.warmup, 1)
                 extra[other] = {"workload": ow.name, "ms_per_step": round(oms, 5),
+                                "ms_per_call": per_call_ms(runner, 64, args.warmup + max(10, min(args.steps, 1500))),
                                 "units_per_s": round(runner.units / (oms / 1e3), 1),
                                 "roofline": roofline(runner.bytes_per_step, oms, other, dominant_kernel(ow))}
                 del ow

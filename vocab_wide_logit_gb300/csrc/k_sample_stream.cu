@@ -589,9 +589,13 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
         }
       }
       // the rest of the slice (at most NT * UNROLL chunks, the row-edge chunk
-      // nq-1 included), one checked chunk per thread and round
+      // nq-1 included), one checked chunk per thread and round; a warp whose
+      // first chunk of the round lies past the slice has none and skips it
 #pragma unroll 1
-      for (int r = 0; r < UNROLL; ++r) batch1(qa + n_full * NT * UNROLL + r * NT + tid, true);
+      for (int r = 0; r < UNROLL; ++r) {
+        const int qw = qa + n_full * NT * UNROLL + r * NT + wid * 32;
+        if (qw < q_hi) batch1(qw + lane, true);
+      }
       if (sampled) {
         if (ns > 0) drain(ns);
         while (ne > 0) eval(min(ne, 32));

@@ -173,7 +173,6 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ SXchg xs;
   __shared__ SRec wrec[NT / 32];
-  __shared__ float2 s_anc[NT / 32];
   __shared__ int s_sa[2];  // best lower-bound score of the cell, per cell parity (ord_enc)
   __shared__ ReqCursor s_cur;
   __shared__ long long s_Pu;
@@ -537,8 +536,10 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
         compute(q0, UN{}, std::false_type{}, STATS{}, true, cc, cu);
       }
       if (sampled) {
-        // Anchor: the CTA's best z so far and its lower-bound score seed SA, so
-        // that the first batch is staged against a useful cut.
+        // Anchor: the warp's best z so far and its lower-bound score seed SA, so
+        // that the first batch is staged against a useful cut. Each warp
+        // publishes its own, with no CTA barrier: the cell's warps start
+        // together, so the others' anchors land in SA within moments.
         float bz = m;
         int bi = am;
 #pragma unroll
@@ -550,22 +551,11 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
             bi = i2;
           }
         }
-        if (lane == 0) s_anc[wid] = make_float2(bz, __int_as_float(bi));
-        __syncthreads();
-#pragma unroll
-        for (int w = 0; w < NT / 32; ++w) {
-          const float2 v = s_anc[w];
-          const int i2 = __float_as_int(v.y);
-          if (v.x > bz || (v.x == bz && i2 < bi)) {
-            bz = v.x;
-            bi = i2;
-          }
-        }
         if (bz > -kInf) bi = chunk_first_id(bi, bz);  // the anchor element of the first chunk holding bz
         if (bz > -kInf && bi != INT_MAX) {
           const uint32_t x = noise_word((uint32_t)bi, t32, cur.rid, ctr3, a.rk0, a.rk1);
           const float lo = __fmaf_rn(tau, gumbel_bounds(x).x, bz);
-          if (wid == 0) publish(lo);
+          publish(lo);
           SAl = fmaxf(SAl, lo);
         }
         if (n_full > 0) compute(q0, UN{}, std::false_type{}, STAGE{}, true, cc, cu);

@@ -233,20 +233,22 @@ def test_exact_ties_at_max_and_at_cut(V):
 
 
 def test_misaligned_rows_and_u_alignment_differing_from_c():
-    """Rows that start at arbitrary 2-byte offsets, with u's rows aligned differently from c's."""
+    """Rows that start at arbitrary 2-byte offsets, with u's rows aligned differently from c's.
+    V = 8192 is a multiple of 8: with aligned buffers every row would start on a chunk boundary,
+    so an offset c buffer, or an offset u buffer alone, must take the general path."""
     dev = _dev()
-    for V in (1025, 5003):
+    for V, c_off, u_off in ((1025, 1, 6), (5003, 1, 6), (8192, 1, 6), (8192, 0, 3)):
         inp = wl.make_sample_inputs("mis", C=2, seq_lens=[3, 4], V=V, guidance=[0.0, 2.0], temperature=[0.9, 0.9],
                                     sigma_c=2.0, sigma_u=1.0, top_ratio=0.1, seed=4)
         d = Dev(inp, dev)
-        cbuf = torch.zeros(inp.c_logits.numel() + 3, dtype=torch.bfloat16, device=dev)
-        cbuf[1:1 + inp.c_logits.numel()] = d.c.reshape(-1)
-        ubuf = torch.zeros(inp.u_logits.numel() + 7, dtype=torch.bfloat16, device=dev)
-        ubuf[6:6 + inp.u_logits.numel()] = d.u.reshape(-1)
-        c_view = cbuf[1:1 + inp.c_logits.numel()].view(inp.C, inp.P, V)
-        u_view = ubuf[6:6 + inp.u_logits.numel()].view(inp.C, inp.P_u, V)
+        cbuf = torch.zeros(inp.c_logits.numel() + 8, dtype=torch.bfloat16, device=dev)
+        cbuf[c_off:c_off + inp.c_logits.numel()] = d.c.reshape(-1)
+        ubuf = torch.zeros(inp.u_logits.numel() + 8, dtype=torch.bfloat16, device=dev)
+        ubuf[u_off:u_off + inp.u_logits.numel()] = d.u.reshape(-1)
+        c_view = cbuf[c_off:c_off + inp.c_logits.numel()].view(inp.C, inp.P, V)
+        u_view = ubuf[u_off:u_off + inp.u_logits.numel()].view(inp.C, inp.P_u, V)
         tok, lp = d.run(8, 2, c=c_view, u=u_view)
-        compare(inp, tok, lp, oracle_cells(inp, 8, 2), label="misaligned V=%d" % V)
+        compare(inp, tok, lp, oracle_cells(inp, 8, 2), label="misaligned V=%d c+%d u+%d" % (V, c_off, u_off))
 
 
 def test_neg_inf_logits():

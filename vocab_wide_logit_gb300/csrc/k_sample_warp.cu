@@ -1,11 +1,12 @@
 // k_sample_warp.cu -- sampling pass for small vocabularies: one warp per cell.
 //
-// A cell's row (V <= 2055) is read once from HBM with 16-byte streaming loads
-// and kept in registers as fp32 z: each lane owns NCH aligned 16-byte chunks
-// (8 elements each) plus at most one scalar element from the unaligned head or
-// tail of the row. Every later step (max, logsumexp, the top-ratio cut, the
-// Gumbel race) runs on-chip. Warps own contiguous cell ranges, so the position
-// -> request walk advances in O(1) per cell.
+// A cell's row (V <= 2055) is read once from HBM: cp.async copies it, in
+// 16-byte chunks, into the warp's shared memory while the previous cell races,
+// and the cell keeps it in registers as fp32 z. Each lane owns NCH aligned
+// 16-byte chunks (8 elements each) plus at most one scalar element from the
+// unaligned head or tail of the row. Every later step (max, logsumexp, the
+// top-ratio cut, the Gumbel race) runs on-chip. Warps own contiguous cell
+// ranges, so the position -> request walk advances in O(1) per cell.
 //
 // Steps per cell ("Sampler support for discrete diffusion", Hert4's first
 // comment; "Add a sampler resource for discrete diffusion", Contract):

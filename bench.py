@@ -244,6 +244,102 @@ def time_steps(runner, steps, warmup, world, timer=None, device="cuda"):
     return ms / steps
 
 
+class PerRequestRunner:
+    """Config 3 through ds_sample_ex: per-request top ratios drawn from {0.05, 0.1, 0.2} and
+    per-request iteration counters (the sampling buffers of a SampleRunner)."""
+
+    def __init__(self, base, dev):
+        self.b = base
+        rng = np.random.Generator(np.random.PCG64(12))
+        B = base.inp.B
+        self.ratios = torch.from_numpy(rng.choice(np.array([0.05, 0.1, 0.2], np.float32), size=B)).to(dev)
+        self.iters = torch.from_numpy(rng.integers(0, 1 << 20, size=B).astype(np.int32)).to(dev)
+
+    def step(self, i):
+        b = self.b
+        b.pkg.ds_sample(b.rid, b.c, b.u, b.sl, b.g, b.tau, b.inp.top_ratio, b.inp.seed, 0, b.tok, b.lp,
+                        top_ratios=self.ratios, iterations=self.iters)
+
+    units = property(lambda self: self.b.inp.cells)
+    bytes_per_step = property(lambda self: self.b.inp.algorithmic_bytes())
+
+
+class RevealRunner:
+    """Confidence ranking and reveal on one config-3 sampling step: every request commits a tenth
+    of its C x T cells (score = the step's logprob)."""
+
+    def __init__(self, base, dev):
+        b = base
+        b.step(0)
+        torch.cuda.synchronize()
+        self.b = b
+        self.scores = b.lp.clone()
+        self.tokens = b.tok.clone()
+        counts = np.ceil(0.1 * b.inp.C * b.inp.seq_lens.astype(np.float64)).astype(np.int32)
+        self.counts = torch.from_numpy(counts).to(dev)
+        self.canvas = torch.full((b.inp.C, b.inp.P), -1, dtype=torch.int32, device=dev)
+        self.revealed = torch.empty((b.inp.C, b.inp.P), dtype=torch.uint8, device=dev)
+        self.n_rev = int(counts.sum())
+
+    def step(self, i):
+        self.b.pkg.ds_reveal(self.scores, self.tokens, self.b.sl, self.counts, self.canvas, self.revealed)
+
+    units = property(lambda self: self.b.inp.cells)
+    # scores read, revealed tokens read and written to the canvas, one flag byte per cell
+    bytes_per_step = property(lambda self: 5 * self.b.inp.cells + 8 * self.n_rev)
+
+
+class LogSoftmaxRunner:
+    """Dense log-softmax of the config-4 rows (rotating input buffers), fp32 or bf16 out."""
+
+    def __init__(self, greedy, dtype):
+        self.g = greedy
+        n, V = greedy.g.n, greedy.g.V
+        self.out = torch.empty((n, V), dtype=dtype, device=greedy.mx.device)
+        self.osize = 4 if dtype == torch.float32 else 2
+
+    def step(self, i):
+        g = self.g
+        g.pkg.ds_log_softmax(g.bufs[i % len(g.bufs)], self.out, g.mx, g.lse, g.am)
+
+    units = property(lambda self: self.g.g.n)
+    bytes_per_step = property(lambda self: self.g.g.n * ((2 + self.osize) * self.g.g.V + 12))
+
+
+class MergeRunner:
+    """Merge of vocabulary-shard triples: 16384 tokens x 8 shards (max, lse, global argmax bits)."""
+
+    def __init__(self, pkg, dev, n=16384, shards=8):
+        self.pkg = pkg
+        rng = np.random.Generator(np.random.PCG64(13))
+        t = np.empty((n, shards, 3), np.float32)
+        t[..., 0] = rng.normal(0.0, 4.0, size=(n, shards))
+        t[..., 1] = t[..., 0] + np.log(rng.uniform(1.0, 3e4, size=(n, shards)))
+        t[..., 2] = rng.integers(0, 248320, size=(n, shards)).astype(np.int32).view(np.float32)
+        self.t = torch.from_numpy(t).to(dev)
+        self.mx = torch.empty(n, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(n, dtype=torch.float32, device=dev)
+        self.am = torch.empty(n, dtype=torch.int32, device=dev)
+        self.n, self.shards = n, shards
+
+    def step(self, i):
+        self.pkg.ds_merge_triples(self.t, self.mx, self.lse, self.am)
+
+    units = property(lambda self: self.n)
+    bytes_per_step = property(lambda self: self.n * (12 * self.shards + 12))
+
+
+def next_row_entry(runner, steps, warmup, workload, note):
+    """Device time and HBM roofline of one next-row entry point (same timing rules as the main line)."""
+    ms = time_steps(runner, steps, warmup, 1)
+    peak, src = hbm_peak()
+    gbs = runner.bytes_per_step / (ms / 1e3) / 1e9
+    return {"workload": workload, "ms_per_call": round(ms, 5),
+            "units_per_s": round(runner.units / (ms / 1e3), 1),
+            "algorithmic_bytes_per_call": runner.bytes_per_step, "achieved_gbs": round(gbs, 1),
+            "frac": round(gbs / peak, 4), "peak": peak, "peak_source": src, "note": note}
+
+
 def per_call_ms(runner, calls, first_step):
     """Median and minimum device time of single calls, one event pair per call, taken after
     (and apart from) the timed region so that its events do not perturb the contract's number."""
@@ -419,6 +515,18 @@ def run_ours(args):
                                     "sample": sample, "host_cpus": os.cpu_count()}
         if not args.no_extra and wname == "cfg3" and world == 1:
             extra = {}
+            nsteps = max(10, min(args.steps, 500))
+            # the next rows built on the path, on the resident config-3 buffers
+            nxt = {
+                "f2_per_request": next_row_entry(
+                    PerRequestRunner(runner, dev), nsteps, args.warmup,
+                    "cfg3 via ds_sample_ex: per-request ratios in {0.05, 0.1, 0.2} and iterations",
+                    "same kernels as the main line; inputs larger than L2"),
+                "f1_reveal": next_row_entry(
+                    RevealRunner(runner, dev), nsteps, args.warmup,
+                    "ds_reveal on one cfg3 step: 64 requests, C = 8, each commits 10% of its cells",
+                    "one CTA per request, 8 radix passes over L2-resident scores: latency-bound"),
+            }
             for other in ("cfg5", "cfg4"):
                 del runner
                 torch.cuda.empty_cache()
@@ -429,7 +537,17 @@ def run_ours(args):
                                 "ms_per_call": per_call_ms(runner, 64, args.warmup + max(10, min(args.steps, 1500))),
                                 "units_per_s": round(runner.units / (oms / 1e3), 1),
                                 "roofline": roofline(runner.bytes_per_step, oms, other, dominant_kernel(ow))}
+                if other == "cfg4":
+                    for dt, nm in ((torch.float32, "f4_log_softmax_f32"), (torch.bfloat16, "f4_log_softmax_bf16")):
+                        nxt[nm] = next_row_entry(
+                            LogSoftmaxRunner(runner, dt), nsteps, args.warmup,
+                            "ds_log_softmax on the cfg4 rows (256 x 248320), %s out" % str(dt).split(".")[-1],
+                            "one read of the logits and one dense write; 4 rotating inputs")
+                    nxt["f3_merge_triples"] = next_row_entry(
+                        MergeRunner(runner.pkg, dev), nsteps, args.warmup,
+                        "ds_merge_triples: 16384 tokens x 8 shards", "1.6 MB, L2-resident: launch-bound")
                 del ow
+            extra["next_rows"] = nxt
             line["also"] = extra
         print(json.dumps(line), flush=True)
     if world > 1:

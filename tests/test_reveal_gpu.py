@@ -51,8 +51,10 @@ def test_reveal_after_sampling_config3():
 
 @pytest.mark.parametrize("levels", [2, 5, 0])
 def test_reveal_with_ties_and_signed_zeros(levels):
+    """Requests of up to 4 x 2049 cells are ranked in shared memory; the 4 x 4500 one (18000 cells,
+    above the staging budget) by the 64-bit select over global memory."""
     rng = np.random.Generator(np.random.PCG64(levels + 40))
-    C, seq_lens = 4, np.array([0, 1, 17, 300, 2049, 64], np.int32)
+    C, seq_lens = 4, np.array([0, 1, 17, 300, 2049, 64, 4500], np.int32)
     P = int(seq_lens.sum())
     if levels:
         scores = (rng.integers(0, levels, size=(C, P)) - levels // 2).astype(np.float32)
@@ -61,7 +63,7 @@ def test_reveal_with_ties_and_signed_zeros(levels):
         scores = rng.standard_normal((C, P)).astype(np.float32)
         scores[0, :50] = -np.inf
     tokens = rng.integers(0, 100000, size=(C, P)).astype(np.int32)
-    counts = np.array([3, 1, 20, 600, 1, C * 64], np.int32)
+    counts = np.array([3, 1, 20, 600, 1, C * 64, 7001], np.int32)
     canvas = rng.integers(-5, 0, size=(C, P)).astype(np.int32)
     got = _run(scores, tokens, seq_lens, counts, canvas)
     want = oracle.reveal(scores, tokens, seq_lens, counts, canvas)

@@ -3,10 +3,13 @@
 // "Sampler support for discrete diffusion" (mstar issue #267), Hert4's first
 // comment: each step scores the whole masked canvas, ranks the cells by
 // confidence over the flattened [C, T] block of a request and commits only the
-// top reveal_count. One CTA per request: an exact radix select finds the
-// reveal_count-th key of the order (score desc, flattened index asc) -- keys
-// are distinct 64-bit words, so exactly that many cells qualify -- and one
-// more pass scatters their tokens into the canvas.
+// top reveal_count. One CTA per request finds the reveal_count-th cell of the
+// order (score desc, flattened index asc) and scatters the tokens of the cells
+// up to it into the canvas. A request of at most kRevealStaged cells is staged
+// once in shared memory as 32-bit score keys: four 8-bit radix rounds find the
+// k-th key H, and the cells tied at H are taken in index order by a prefix
+// count. A larger request runs an exact 64-bit radix select (score key above
+// the inverted flattened index, so keys are distinct) over global memory.
 #include <climits>
 
 #include "ds_device.cuh"
@@ -16,13 +19,43 @@ namespace ds {
 
 namespace {
 
-constexpr int kRevealNT = 256;
+constexpr int kRevealNT = 1024;  // short passes: a request holds about 2000 cells
+constexpr int kRevealStaged = 16384;  // cells staged in shared memory (64 KB of keys)
 
 // Larger key = earlier in the reveal order: the score's order-preserving bits
 // (-0 folded onto +0, so equal scores tie) above the inverted flattened index.
+__device__ __forceinline__ uint32_t score_key(float s) { return order_key((s == 0.f) ? 0.f : s); }
 __device__ __forceinline__ unsigned long long reveal_key(float s, uint32_t f) {
-  const float sc = (s == 0.f) ? 0.f : s;
-  return ((unsigned long long)order_key(sc) << 32) | (unsigned long long)(0xffffffffu - f);
+  return ((unsigned long long)score_key(s) << 32) | (unsigned long long)(0xffffffffu - f);
+}
+
+// Warp 0 finds the digit of the need-th largest key from a 256-bin histogram:
+// bins in descending digit order, lane l holding digits 255-8l .. 248-8l.
+// Returns (digit, keys above it) in lane src; the caller broadcasts.
+__device__ __forceinline__ void pick_digit(const int* hist, int need, int lane, int& digit, int& above) {
+  int cl[8], sum = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    cl[e] = hist[255 - 8 * lane - e];
+    sum += cl[e];
+  }
+  const int above_lane = warp_excl_scan(sum, lane);
+  const bool here = above_lane < need && need <= above_lane + sum;
+  const int src = __ffs(__ballot_sync(0xffffffffu, here)) - 1;
+  digit = -1;
+  above = 0;
+  if (lane == src) {
+    int run = above_lane;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (run + cl[e] >= need) {
+        digit = 255 - 8 * lane - e;
+        above = run;
+        break;
+      }
+      run += cl[e];
+    }
+  }
 }
 
 }  // namespace
@@ -38,6 +71,8 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
   __shared__ int s_bad;
   __shared__ unsigned long long s_prefix;
   __shared__ int s_need;
+  __shared__ int s_wcnt[kRevealNT / 32];
+  extern __shared__ uint32_t skeys[];  // the staged request's score keys, in flattened order
   pdl_release();
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -77,6 +112,65 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
       return c * (long long)P + roff + (f - c * T);
     };
 
+    if (k > 0 && k < n && n <= kRevealStaged) {
+      const int nn = (int)n, kk = (int)k;
+      for (int f = tid; f < nn; f += kRevealNT) skeys[f] = score_key(scores[cell_of(f)]);
+      if (tid == 0) {
+        s_prefix = 0ull;
+        s_need = kk;
+      }
+      __syncthreads();
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int b = tid; b < 256; b += kRevealNT) hist[b] = 0;
+        __syncthreads();
+        const uint32_t prefix = (uint32_t)s_prefix;
+        for (int f = tid; f < nn; f += kRevealNT) {
+          const uint32_t key = skeys[f];
+          if (shift == 24 || (key >> (shift + 8)) == (prefix >> (shift + 8))) atomicAdd(&hist[(key >> shift) & 255u], 1);
+        }
+        __syncthreads();
+        if (wid == 0) {
+          int digit, above;
+          pick_digit(hist, s_need, lane, digit, above);
+          if (digit >= 0) {
+            s_prefix = (unsigned long long)(prefix | ((uint32_t)digit << shift));
+            s_need -= above;
+          }
+        }
+        __syncthreads();
+      }
+      // every key above H is revealed; of the keys equal to H, the first `need`
+      // in flattened order (a running count over chunks of kRevealNT cells)
+      const uint32_t H = (uint32_t)s_prefix;
+      const int need = s_need;
+      int run = 0;
+      for (int base = 0; base < nn; base += kRevealNT) {
+        const int f = base + tid;
+        const uint32_t key = (f < nn) ? skeys[f] : 0u;
+        const bool tied = f < nn && key == H;
+        const unsigned bt = __ballot_sync(0xffffffffu, tied);
+        if (lane == 0) s_wcnt[wid] = __popc(bt);
+        __syncthreads();
+        int before = run, total = 0;
+#pragma unroll
+        for (int w = 0; w < kRevealNT / 32; ++w) {
+          const int cw = s_wcnt[w];
+          before += (w < wid) ? cw : 0;
+          total += cw;
+        }
+        before += __popc(bt & ((1u << lane) - 1u));
+        if (f < nn) {
+          const bool on = key > H || (tied && before < need);
+          const long long cell = cell_of(f);
+          if (on) canvas[cell] = tokens[cell];
+          if (revealed) revealed[cell] = on ? 1 : 0;
+        }
+        run += total;
+        __syncthreads();  // s_wcnt is rewritten by the next chunk
+      }
+      continue;  // uniform across the CTA
+    }
+
     unsigned long long kth = 0ull;  // with k > 0, every key >= kth is revealed
     if (k > 0 && k < n) {
       if (tid == 0) {
@@ -94,28 +188,11 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
         }
         __syncthreads();
         if (wid == 0) {
-          // bins in descending digit order: lane l holds digits 255-8l .. 248-8l
-          int cl[8], sum = 0;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            cl[e] = hist[255 - 8 * lane - e];
-            sum += cl[e];
-          }
-          const int need = s_need;
-          const int above_lane = warp_excl_scan(sum, lane);
-          const bool here = above_lane < need && need <= above_lane + sum;
-          const int src = __ffs(__ballot_sync(0xffffffffu, here)) - 1;
-          if (lane == src) {
-            int run = above_lane;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              if (run + cl[e] >= need) {
-                s_prefix = prefix | ((unsigned long long)(255 - 8 * lane - e) << shift);
-                s_need = need - run;
-                break;
-              }
-              run += cl[e];
-            }
+          int digit, above;
+          pick_digit(hist, s_need, lane, digit, above);
+          if (digit >= 0) {
+            s_prefix = prefix | ((unsigned long long)digit << shift);
+            s_need -= above;
           }
         }
         __syncthreads();
@@ -141,12 +218,16 @@ cudaError_t launch_reveal(const float* scores, const int32_t* tokens, const int3
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_reveal, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(kRevealStaged * sizeof(uint32_t)));
+  if (e != cudaSuccess) return e;
   long long blocks = B;
   if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
   if (blocks < 1) blocks = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks, 1, 1);
   cfg.blockDim = dim3(kRevealNT, 1, 1);
+  cfg.dynamicSmemBytes = kRevealStaged * sizeof(uint32_t);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

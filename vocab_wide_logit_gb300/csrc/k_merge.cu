@@ -48,65 +48,75 @@ __global__ void __launch_bounds__(256) k_merge_triples(const float* __restrict__
 }
 
 // Dense log-softmax write-out: out[row][i] = x[row][i] - lse[row], fp32 or bf16
-// (round to nearest even). One grid-stride pass over 16-byte chunks of the
-// row-major [n][V] matrix; rows need not be 16-byte aligned, so chunk edges are
-// handled element by element.
+// (round to nearest even). Blocks stride over rows (blockIdx.y) and, within a
+// row, over its 16-byte chunks of x (blockIdx.x), so a row's lse is read once
+// and no flat index is divided. A row whose x and out both reach a 16-byte
+// boundary after the same h head elements goes by chunks, four in flight per
+// thread, with its head and tail element by element; any other row goes
+// element by element.
 template <bool BF16_OUT>
 __global__ void __launch_bounds__(256) k_log_softmax_write(const uint16_t* __restrict__ x, int n, int V,
                                                            const float* __restrict__ lse, void* __restrict__ out) {
   pdl_release();
   pdl_wait();
-  const long long total = (long long)n * V;
-  const long long n8 = total >> 3;
-  const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
-                       (reinterpret_cast<uintptr_t>(out) & 15) == 0;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < (aligned ? n8 : 0); c += stride) {
-    const uint4 v = ld_stream16(reinterpret_cast<const uint4*>(x) + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float f[8];
-    const long long e0 = c * 8;
-    int row = (int)(e0 / V);
-    int col = (int)(e0 - (long long)row * V);
-    float l = lse[row];
+  constexpr int OB = BF16_OUT ? 2 : 4;  // output bytes per element
+  const int tpr = gridDim.x * blockDim.x;  // threads per row
+  const int tr = blockIdx.x * blockDim.x + threadIdx.x;
+  for (int row = blockIdx.y; row < n; row += gridDim.y) {
+    const float l = lse[row];
+    const uint16_t* xr = x + (long long)row * V;
+    unsigned char* orow = reinterpret_cast<unsigned char*>(out) + (long long)row * V * OB;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(xr), oa = reinterpret_cast<uintptr_t>(orow);
+    const int h = min((int)(((16u - (unsigned)(xa & 15)) & 15u) >> 1), V);
+    const bool vec = ((oa + (uintptr_t)h * OB) & 15) == 0;
+    const int nfc = vec ? (V - h) >> 3 : 0;
+    const uint4* xc = reinterpret_cast<const uint4*>(xr + h);
+    unsigned char* oc = orow + (long long)h * OB;
+    for (int q0 = tr; q0 < nfc; q0 += 4 * tpr) {
+      uint4 v[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = bf_lo(w[i]);
-      f[2 * i + 1] = bf_hi(w[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (col == V) {  // the chunk runs into the next row
-        ++row;
-        col = 0;
-        l = lse[row];
+      for (int u = 0; u < 4; ++u) {
+        const int q = q0 + u * tpr;
+        v[u] = (q < nfc) ? ld_stream16(xc + q) : make_uint4(0u, 0u, 0u, 0u);
       }
-      f[i] -= l;
-      ++col;
-    }
-    if (BF16_OUT) {
-      uint32_t o[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+      for (int u = 0; u < 4; ++u) {
+        const int q = q0 + u * tpr;
+        if (q < nfc) {
+          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          float f[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            f[2 * i] = bf_lo(w[i]) - l;
+            f[2 * i + 1] = bf_hi(w[i]) - l;
+          }
+          if (BF16_OUT) {
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const __nv_bfloat162 hh = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+              o[i] = *reinterpret_cast<const uint32_t*>(&hh);
+            }
+            reinterpret_cast<uint4*>(oc)[q] = make_uint4(o[0], o[1], o[2], o[3]);
+          } else {
+            float4* o = reinterpret_cast<float4*>(oc) + 2 * q;
+            o[0] = make_float4(f[0], f[1], f[2], f[3]);
+            o[1] = make_float4(f[4], f[5], f[6], f[7]);
+          }
+        }
       }
-      reinterpret_cast<uint4*>(out)[c] = make_uint4(o[0], o[1], o[2], o[3]);
-    } else {
-      float4* o = reinterpret_cast<float4*>(out) + 2 * c;
-      o[0] = make_float4(f[0], f[1], f[2], f[3]);
-      o[1] = make_float4(f[4], f[5], f[6], f[7]);
     }
-  }
-  // element-wise: the tail after the last whole chunk, or everything when unaligned
-  for (long long e = (aligned ? n8 * 8 : 0) + blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
-       e += stride) {
-    const int row = (int)(e / V);
-    const float v = __uint_as_float((uint32_t)x[e] << 16) - lse[row];
-    if (BF16_OUT)
-      reinterpret_cast<__nv_bfloat16*>(out)[e] = __float2bfloat16_rn(v);
-    else
-      reinterpret_cast<float*>(out)[e] = v;
+    // element by element: the head and the tail of a chunked row, or the whole row
+    const int tail0 = h + 8 * nfc;
+    const int ne = vec ? h + (V - tail0) : V;
+    for (int j = tr; j < ne; j += tpr) {
+      const int e = (vec && j >= h) ? tail0 + (j - h) : j;
+      const float v = __uint_as_float((uint32_t)xr[e] << 16) - l;
+      if (BF16_OUT)
+        reinterpret_cast<__nv_bfloat16*>(orow)[e] = __float2bfloat16_rn(v);
+      else
+        reinterpret_cast<float*>(orow)[e] = v;
+    }
   }
 }
 
@@ -142,10 +152,34 @@ cudaError_t launch_merge_triples(const float* triples, int n, int shards, float*
 
 cudaError_t launch_log_softmax_write(const uint16_t* x, int n, int V, const float* lse, void* out, bool bf16_out,
                                      cudaStream_t st) {
+  if (n <= 0 || V <= 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // rows on y; per row enough blocks on x that the grid holds about 8 blocks per
+  // SM, but no more than the row's chunks need at 4 per thread
+  const int by = n < 65535 ? n : 65535;
+  const long long want = ((long long)sms * 8 + by - 1) / by;
+  const long long need = ((long long)V / 8 + 4 * 256 - 1) / (4 * 256);
+  long long bx = want < need ? want : need;
+  if (bx < 1) bx = 1;
   void* args[] = {&x, &n, &V, &lse, &out};
-  const long long work = ((long long)n * V + 7) / 8;
-  return bf16_out ? launch_plain(reinterpret_cast<const void*>(&k_log_softmax_write<true>), args, work, st)
-                  : launch_plain(reinterpret_cast<const void*>(&k_log_softmax_write<false>), args, work, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)bx, (unsigned)by, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const void* kern = bf16_out ? reinterpret_cast<const void*>(&k_log_softmax_write<true>)
+                              : reinterpret_cast<const void*>(&k_log_softmax_write<false>);
+  e = cudaLaunchKernelExC(&cfg, kern, args);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace ds

@@ -191,8 +191,12 @@ ds_status ds_merge_triples(const float* triples, int32_t n, int32_t shards, floa
  * Defined by: the dense fallback path of "perf: avoid full-vocab all-gather
  * for draft greedy sampling" (LightLLM PR #1517), Design and invariants, for
  * callers that still need full log-probabilities: out[r][i] = x[r][i] -
- * logsumexp(x[r]). It runs ds_greedy_lse and then one pass that re-reads the
- * logits and writes 4 (fp32) or 2 (bf16) bytes per element.
+ * logsumexp(x[r]). A row of up to about 262k logits is held in the shared
+ * memory of a thread-block cluster, so the logits are read once and 4 (fp32)
+ * or 2 (bf16) bytes per element are written. A longer row runs ds_greedy_lse
+ * and then a pass that re-reads the logits. The triple equals ds_greedy_lse's
+ * in max and argmax; lse agrees with it to fp32 rounding (the sums are taken
+ * in another order).
  *
  * Arguments:
  *   logits      device bf16 [n][V], V contiguous, 2-byte alignment.

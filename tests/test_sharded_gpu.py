@@ -85,10 +85,12 @@ def test_merge_against_the_oracle_merge_with_empty_shards():
     assert float(mm[5]) == -np.inf and float(ml[5]) == -np.inf
 
 
-@pytest.mark.parametrize("V", [1, 7, 1025, 4097, 248320])
+@pytest.mark.parametrize("V", [1, 7, 1025, 4097, 248320, 300000])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("offset", [0, 1])
 def test_dense_log_softmax_matches_the_oracle(V, dtype, offset):
+    """Rows up to about 262k logits are held on chip by a cluster (one read); V = 300000 takes the
+    two-pass form (the triple pass, then the write pass)."""
     dev = _dev()
     n = 6 if V > 5000 else 9
     g = wl.make_greedy_inputs("lsm", n=n, V=V, sigma=3.0, seed=V % 97, tie_fraction=0.0)
@@ -99,7 +101,10 @@ def test_dense_log_softmax_matches_the_oracle(V, dtype, offset):
     out, mx, lse, am = pkg.log_softmax(x, dtype=dtype)
     gm, gl, ga = pkg.greedy_lse(x)
     torch.cuda.synchronize()
-    assert torch.equal(mx, gm) and torch.equal(am, ga) and torch.equal(lse, gl)
+    # max and argmax are exact; lse is summed in another order than the greedy pass, so
+    # the two agree to fp32 rounding (each is held to the oracle's double lse below)
+    assert torch.equal(mx, gm) and torch.equal(am, ga)
+    assert torch.allclose(lse, gl, rtol=1e-6, atol=1e-6)
     ref = oracle.greedy_rows(wl.bf16_bits(g.logits), n, V)
     xs = g.logits.float().numpy().astype(np.float64)
     want = xs - ref["lse"][:, None]

@@ -184,8 +184,16 @@ ds_status ds_log_softmax(const void* logits, int32_t n, int32_t V, void* out, in
     return DS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const uint16_t* x = static_cast<const uint16_t*>(logits);
-  cudaError_t e = ds::launch_greedy(x, n, V, out_max, out_lse, out_argmax, st);
-  if (e == cudaSuccess) e = ds::launch_log_softmax_write(x, n, V, out_lse, out, out_dtype == DS_DTYPE_BF16, st);
+  const bool bf16_out = out_dtype == DS_DTYPE_BF16;
+  cudaError_t e;
+  if (ds::log_softmax_fused_fits(V)) {
+    // the row held on chip by a cluster: one read of the logits
+    e = ds::launch_log_softmax_fused(x, n, V, out_max, out_lse, out_argmax, out, bf16_out, st);
+  } else {
+    // the triple pass, then the write pass (a second read of the logits)
+    e = ds::launch_greedy(x, n, V, out_max, out_lse, out_argmax, st);
+    if (e == cudaSuccess) e = ds::launch_log_softmax_write(x, n, V, out_lse, out, bf16_out, st);
+  }
   return e == cudaSuccess ? DS_OK : DS_ERR_CUDA;
 }
 

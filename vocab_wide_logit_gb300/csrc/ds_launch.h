@@ -31,4 +31,10 @@ cudaError_t launch_reveal(const float* scores, const int32_t* tokens, const int3
 cudaError_t launch_log_softmax_write(const uint16_t* x, int n, int V, const float* lse, void* out, bool bf16_out,
                                      cudaStream_t st);
 
+// Dense log-softmax with each row held in a cluster's shared memory (one read of
+// the logits); fits when a row splits into at most 8 slices of 64 KB.
+bool log_softmax_fused_fits(int V);
+cudaError_t launch_log_softmax_fused(const uint16_t* x, int n, int V, float* out_max, float* out_lse,
+                                     int* out_argmax, void* out, bool bf16_out, cudaStream_t st);
+
 }  // namespace ds

@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
     // ---- race state (queue lengths and flags are warp-uniform)
     float m = -kInf, s = 0.f;
     int am = INT_MAX;  // first chunk holding m
+    int aid = INT_MAX;  // id of the first element equal to m (read by the anchor only)
     float SAl = -kInf;           // best lower-bound score this warp knows of
     int ns = 0, ne = 0, nl = 0;  // staged chunks, queued elements, live elements
     int E = 0;                   // elements this warp sent to the noise stage
@@ -476,11 +477,22 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
             // an equal max met later has larger ids)
             s = (m == -kInf) ? 0.f : s * ex2_approx((m - bm) * kLog2e);
             m = bm;
-            int aa = INT_MAX;
+            int aa = INT_MAX, ai = INT_MAX;
 #pragma unroll
-            for (int uu = NCHK - 1; uu >= 0; --uu)
-              if (cmx[uu] == bm) aa = q0 + uu * NT;
+            for (int uu = NCHK - 1; uu >= 0; --uu) {
+              if (cmx[uu] == bm) {
+                aa = q0 + uu * NT;
+                int e = 0;
+#pragma unroll
+                for (int i = 3; i >= 0; --i) {
+                  if (z[uu][i].y == bm) e = 2 * i + 1;
+                  if (z[uu][i].x == bm) e = 2 * i;
+                }
+                ai = 8 * aa - dc + e;
+              }
+            }
             am = aa;
+            aid = ai;
           }
           if (m != -kInf) {
             const float2 nml = make_float2(-m * kLog2e, -m * kLog2e);
@@ -541,7 +553,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
         // publishes its own, with no CTA barrier: the cell's warps start
         // together, so the others' anchors land in SA within moments.
         float bz = m;
-        int bi = am;
+        int bi = aid;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
           const float z2 = __shfl_xor_sync(0xffffffffu, bz, o);
@@ -551,8 +563,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
             bi = i2;
           }
         }
-        if (bz > -kInf) bi = chunk_first_id(bi, bz);  // the anchor element of the first chunk holding bz
-        if (bz > -kInf && bi != INT_MAX) {
+        if (bz > -kInf && bi != INT_MAX) {  // the warp's first element holding its max
           const uint32_t x = noise_word((uint32_t)bi, t32, cur.rid, ctr3, a.rk0, a.rk1);
           const float lo = __fmaf_rn(tau, gumbel_bounds(x).x, bz);
           publish(lo);

@@ -224,9 +224,11 @@ def max_over_ranks(ms, world, device):
     return float(t.item())
 
 
-def time_steps(runner, steps, warmup, world, timer=None, device="cuda"):
+def time_steps(runner, steps, warmup, world, timer=None, device="cuda", counter=None):
     """W untimed steps, then exactly K timed steps bracketed by a barrier and a device
-    synchronisation on both sides; returns ms per step, the max over ranks."""
+    synchronisation on both sides; returns ms per step, the max over ranks. With a launch
+    counter (the library's ds_launch_count), the kernels launched inside the timed region
+    are left in runner.timed_launches."""
     timer = timer or DeviceTimer()
     for i in range(warmup):
         runner.step(i)
@@ -234,10 +236,13 @@ def time_steps(runner, steps, warmup, world, timer=None, device="cuda"):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    c0 = counter() if counter else 0
     timer.start()
     for i in range(steps):
         runner.step(warmup + i)
     ms = timer.stop()
+    if counter:
+        runner.timed_launches = counter() - c0
     ms = max_over_ranks(ms, world, device)
     if world > 1:
         torch.distributed.barrier()
@@ -355,26 +360,18 @@ def per_call_ms(runner, calls, first_step):
     return {"median": round(statistics.median(t), 5), "min": round(t[0], 5), "calls": calls}
 
 
-def launches_per_step(w):
-    """Kernels one ds_sample / ds_greedy_lse call launches (mirrors the library's dispatch:
-    one warp-per-cell kernel up to V = 2055; the streaming kernel plus its fix-up pass when
-    4k <= V; the staged cluster kernel otherwise; one greedy kernel)."""
-    if not hasattr(w, "top_ratio"):
-        return 1
-    if w.V <= 2055:
-        return 1
-    import vocab_wide_logit_gb300 as pkg
-    k = pkg.top_k(w.top_ratio, w.V)
-    return 2 if 4 * k <= w.V else 1
-
-
 def dominant_kernel(w):
+    """The kernel that carries a call (mirrors the library's dispatch: the warp-per-cell kernel up
+    to V = 2055; the streaming kernel, in one or two launches, plus its fix-up pass when 4k <= V;
+    the staged cluster kernel otherwise; the greedy kernel)."""
     if not hasattr(w, "top_ratio"):
         return "k_greedy_lse"
     if w.V <= 2055:
         return "k_sample_warp"
+    import vocab_wide_logit_gb300 as pkg
+    k = pkg.top_k(w.top_ratio, w.V)
     return "k_sample_stream (+ fix-up k_sample_cluster in the same timed step)" \
-        if launches_per_step(w) == 2 else "k_sample_cluster"
+        if 4 * k <= w.V else "k_sample_cluster"
 
 
 def oracle_cpu_rate(inp, max_seconds=10.0, iteration=0):
@@ -479,7 +476,7 @@ def run_ours(args):
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[dev.index]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else dev.index
     with ClockSampler(gpu_index) as clk:
-        ms = time_steps(runner, args.steps, args.warmup, world)
+        ms = time_steps(runner, args.steps, args.warmup, world, counter=pkg.launch_count)
     clocks = clk.summary()
     units = runner.units * world
     value = units / (ms / 1e3)
@@ -491,7 +488,7 @@ def run_ours(args):
         "dtype": "f32", "data": "synthetic (seeded, bf16 inputs)",
         "config": run_config(w, is_greedy, world),
         "roofline": roofline(runner.bytes_per_step, ms, wname, dominant_kernel(w)),
-        "gpu_launches": args.steps * launches_per_step(w),
+        "gpu_launches": runner.timed_launches,
         "clocks": clocks,
     }
     if rank == 0 and not is_greedy:

@@ -254,6 +254,12 @@ const char* ds_status_string(ds_status s);
  * 0 when the arguments are invalid. Host-only, no CUDA call. */
 int32_t ds_top_k(float top_ratio, int32_t V);
 
+/* Number of kernels the library has launched in this process so far (every
+ * successful launch by any entry point adds one; a call may launch one to three
+ * kernels depending on its sizes and the device). For accounting by callers such
+ * as benchmarks. Host-only, thread-safe, no CUDA call. */
+uint64_t ds_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

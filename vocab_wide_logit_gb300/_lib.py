@@ -21,7 +21,7 @@ DS_DEV_ERR_PARAM = 4
 DS_MAX_VOCAB = 262137
 
 EXPORTED = ("ds_sample", "ds_greedy_lse", "ds_status_string", "ds_top_k", "ds_merge_triples", "ds_log_softmax",
-            "ds_reveal", "ds_sample_ex")
+            "ds_reveal", "ds_sample_ex", "ds_launch_count")
 DS_FLAG_KEEP_TIES = 1
 DS_DTYPE_F32 = 0
 DS_DTYPE_BF16 = 1
@@ -53,6 +53,8 @@ def load(path: str = LIB_PATH):
     L.ds_status_string.restype = ctypes.c_char_p
     L.ds_top_k.argtypes = [f32, i32]
     L.ds_top_k.restype = i32
+    L.ds_launch_count.argtypes = []
+    L.ds_launch_count.restype = ctypes.c_uint64
     L.ds_merge_triples.argtypes = [vp, i32, i32, vp, vp, vp, vp]
     L.ds_merge_triples.restype = ctypes.c_int
     L.ds_log_softmax.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp]
@@ -72,6 +74,11 @@ def status_string(code: int) -> str:
 
 def top_k(top_ratio: float, V: int) -> int:
     return int(load().ds_top_k(float(top_ratio), int(V)))
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process so far (ds_launch_count)."""
+    return int(load().ds_launch_count())
 
 
 def _ptr(t):

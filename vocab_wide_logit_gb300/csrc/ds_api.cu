@@ -4,6 +4,7 @@
 // and the two normal quantiles that seed the kernels' threshold guesses, pick
 // the kernel by vocabulary size, and launch asynchronously on the caller's
 // stream. Nothing is allocated and nothing is synchronised.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -43,9 +44,17 @@ int device_sm_count() {
   return cached_sms;
 }
 
+std::atomic<unsigned long long> g_launches{0};
+
 }  // namespace
 
+namespace ds {
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace ds
+
 extern "C" {
+
+uint64_t ds_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* ds_status_string(ds_status s) {
   switch (s) {

@@ -8,6 +8,9 @@
 
 namespace ds {
 
+// Counts every kernel the library launches (read by ds_launch_count).
+void note_launch();
+
 constexpr int kWarpKernelThreads = 128;
 constexpr int kStreamMark = -2;  // out_tokens marker left by the streaming kernel for the staged one
 

@@ -254,6 +254,7 @@ cudaError_t launch_greedy(const uint16_t* x, int n, int V, float* out_max, float
   cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, x, n, V, out_max, out_lse, out_argmax);
   if (e != cudaSuccess) return e;
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -321,6 +321,7 @@ cudaError_t launch_log_softmax_fused(const uint16_t* x, int n, int V, float* out
   cfg.gridDim = dim3((unsigned)(n_clusters * cs), 1, 1);
   e = cudaLaunchKernelEx(&cfg, kern, x, n, V, out_max, out_lse, out_argmax, out);
   if (e != cudaSuccess) return e;
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -141,6 +141,7 @@ static cudaError_t launch_plain(const void* kern, void** args, long long work, c
   cfg.numAttrs = 1;
   e = cudaLaunchKernelExC(&cfg, kern, args);
   if (e != cudaSuccess) return e;
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -179,6 +180,7 @@ cudaError_t launch_log_softmax_write(const uint16_t* x, int n, int V, const floa
                               : reinterpret_cast<const void*>(&k_log_softmax_write<false>);
   e = cudaLaunchKernelExC(&cfg, kern, args);
   if (e != cudaSuccess) return e;
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -237,6 +237,7 @@ cudaError_t launch_reveal(const float* scores, const int32_t* tokens, const int3
   e = cudaLaunchKernelEx(&cfg, k_reveal, scores, tokens, seq_lens, reveal_counts, B, C, P, canvas, revealed,
                          d_status);
   if (e != cudaSuccess) return e;
+  note_launch();
   return cudaGetLastError();
 }
 

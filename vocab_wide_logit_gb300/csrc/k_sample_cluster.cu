@@ -719,6 +719,7 @@ cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st, int only
   cfg.gridDim = dim3((unsigned)(n_clusters * cs), 1, 1);
   e = cudaLaunchKernelEx(&cfg, kern, a, slice_cap, only_marked);
   if (e != cudaSuccess) return e;
+  note_launch();
   return cudaGetLastError();
 }
 

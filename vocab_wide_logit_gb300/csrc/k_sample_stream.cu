@@ -33,6 +33,7 @@
 // is then also the kept-set winner. A cell that fails this (or fills a live
 // list) is marked in out_tokens and finished exactly by the staged kernel
 // launched right after.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 #include <cooperative_groups.h>
@@ -168,7 +169,7 @@ constexpr float kExactGFrom = 6.0f;
 // both buffers 16-byte aligned), so chunks never straddle rows and u never
 // needs the element-wise gather.
 template <int NT, int UNROLL, bool ALIGNED>
-__global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
+__global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, long long cell_lo, long long cell_hi) {
   pdl_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ SXchg xs;
@@ -184,7 +185,6 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
   WarpArea& W = reinterpret_cast<WarpArea*>(smem_raw)[wid];
-  const long long n_cells = (long long)a.C * a.P;
   const long long n_clusters = (long long)gridDim.x / cs;
   const long long cluster_id = (long long)blockIdx.x / cs;
   const int P = a.P, V = a.V;
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
   __syncthreads();
   if (s_bad) {
     if (rank == 0 && tid == 0) {
-      for (long long cell = cluster_id; cell < n_cells; cell += n_clusters) {
+      for (long long cell = cell_lo + cluster_id; cell < cell_hi; cell += n_clusters) {
         a.out_tokens[cell] = -1;
         a.out_logprobs[cell] = __int_as_float(0x7fc00000);
       }
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
   const float g_min = kGumbelBounds[0].x;
 
   int it = 0;
-  for (long long cell = cluster_id; cell < n_cells; cell += n_clusters, ++it) {
+  for (long long cell = cell_lo + cluster_id; cell < cell_hi; cell += n_clusters, ++it) {
     const int c = (int)(cell / P);
     const int p = (int)(cell - (long long)c * P);
     const int slot = it & 1;
@@ -706,11 +706,52 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a) {
 }
 
 // ---------------------------------------------------------------- launcher
+namespace {
+
+// Clusters of cs CTAs that fit on the device at once (cached per device, row
+// alignment and cluster size; the answer depends on the kernel's resources only).
+int stream_capacity(int dev, bool aligned, int cs, const void* kern, size_t smem) {
+  static std::atomic<int> cache[16][2][3];
+  const int ci = cs == 1 ? 0 : (cs == 2 ? 1 : 2);
+  if (dev >= 0 && dev < 16) {
+    const int v = cache[dev][aligned][ci].load(std::memory_order_relaxed);
+    if (v != 0) return v;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kStreamNT, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3((unsigned)cs, 1, 1);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return -1;
+  if (dev >= 0 && dev < 16) cache[dev][aligned][ci].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// CTA time per cell relative to one CTA per cell, measured on GB300 at
+// V = 248320 (1024 cells): 1.00, 1.10 and 1.19 for 1, 2 and 4 CTAs. A cell
+// split over more CTAs finishes sooner but waits on more warps at its merge.
+double stream_cell_cost(int cs) { return cs == 1 ? 1.0 : (cs == 2 ? 1.10 : 1.19); }
+
+}  // namespace
+
+// Up to two launches: the cheapest of one launch with 1, 2 or 4 CTAs per cell,
+// or full rounds of one CTA per cell followed by the remaining cells on 2 or 4
+// CTAs each (so that a partial last round still fills the GPU). Time in units
+// of one CTA on one cell: rounds x cost(cs) / cs.
 cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
+  const long long n_cells = (long long)a.C * a.P;
+  if (n_cells <= 0) return cudaSuccess;
   const int nq_max = (a.V + 7 + 7) >> 3;
-  // up to 4 CTAs per row: enough logits per thread to amortise the per-cell rounds
-  int cs = 1;
-  while (cs < 4 && nq_max / cs > 2 * kStreamNT * kStreamUnroll) cs *= 2;
+  // at most 4 CTAs per row, and no more than leave each CTA about two batches per thread
+  int cs_max = 1;
+  while (cs_max < 4 && nq_max / cs_max > 2 * kStreamNT * kStreamUnroll) cs_max *= 2;
   const bool aligned = (a.V % 8) == 0 && (reinterpret_cast<uintptr_t>(a.c) & 15) == 0 &&
                        (reinterpret_cast<uintptr_t>(a.u) & 15) == 0;
   auto kern = aligned ? k_sample_stream<kStreamNT, kStreamUnroll, true>
@@ -718,31 +759,66 @@ cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(WarpArea) * (kStreamNT / 32);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kStreamNT, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  cfg.gridDim = dim3((unsigned)cs, 1, 1);
-  int max_clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+  int dev = 0;
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (max_clusters < 1) return cudaErrorLaunchOutOfResources;
-  const long long n_cells = (long long)a.C * a.P;
-  long long n_clusters = max_clusters;
-  if (n_clusters > n_cells) n_clusters = n_cells;
-  cfg.gridDim = dim3((unsigned)(n_clusters * cs), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, a);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  long long cap[5] = {0, 0, 0, 0, 0};
+  for (int cs = 1; cs <= cs_max; cs *= 2) {
+    cap[cs] = stream_capacity(dev, aligned, cs, reinterpret_cast<const void*>(kern), smem);
+    if (cap[cs] < 1) return cudaErrorLaunchOutOfResources;
+  }
+  auto t_of = [&](int cs, long long cells) {
+    return (double)((cells + cap[cs] - 1) / cap[cs]) * stream_cell_cost(cs) / cs;
+  };
+  // the plan: cs1 for cells [0, split), cs2 for [split, n_cells)
+  int cs1 = 1, cs2 = 1;
+  long long split = n_cells;
+  double best = t_of(1, n_cells);
+  for (int cs = 2; cs <= cs_max; cs *= 2) {
+    const double t = t_of(cs, n_cells);
+    if (t < best) {
+      best = t;
+      cs1 = cs;
+      split = n_cells;
+    }
+  }
+  const long long full = (n_cells / cap[1]) * cap[1];
+  if (full > 0 && full < n_cells) {
+    for (int cs = 2; cs <= cs_max; cs *= 2) {
+      const double t = (double)(full / cap[1]) + t_of(cs, n_cells - full);
+      if (t < best) {
+        best = t;
+        cs1 = 1;
+        cs2 = cs;
+        split = full;
+      }
+    }
+  }
+  auto launch = [&](int cs, long long lo, long long hi) -> cudaError_t {
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kStreamNT, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    long long n_clusters = cap[cs];
+    if (n_clusters > hi - lo) n_clusters = hi - lo;
+    cfg.gridDim = dim3((unsigned)(n_clusters * cs), 1, 1);
+    cudaError_t r = cudaLaunchKernelEx(&cfg, kern, a, lo, hi);
+    if (r != cudaSuccess) return r;
+    note_launch();
+    return cudaGetLastError();
+  };
+  e = launch(cs1, 0, split);
+  if (e == cudaSuccess && split < n_cells) e = launch(cs2, split, n_cells);
+  return e;
 }
 
 }  // namespace ds

@@ -733,6 +733,7 @@ static cudaError_t launch_nch(const SampleArgs& a, cudaStream_t st, int num_sms)
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, k_sample_warp<NCH>, a);
   if (e != cudaSuccess) return e;
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -606,11 +606,12 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
     // ---- threshold guess from the subsample moments
     float tlo = -FLT_MAX;  // -FLT_MAX: keep every finite element
     bool guessed = false;
+    float sd = 0.f;
     if (NCH >= 2 && G.q_lo > -kInf) {
       const float inv_n = 1.0f / (float)(32 * 8 * (NCH > 1 ? NCH - 1 : 1));  // power of two: exact
       const float S1 = warp_sum(s1.x + s1.y), S2 = warp_sum(s2.x + s2.y);
       const float mu = S1 * inv_n;
-      const float sd = sqrtf(fmaxf(fmaf(S2, inv_n, -mu * mu), 0.f));
+      sd = sqrtf(fmaxf(fmaf(S2, inv_n, -mu * mu), 0.f));
       const float guess = fmaf(sd, G.q_lo, mu);
       if (isfinite(guess)) {
         tlo = fminf(guess, m);
@@ -648,9 +649,14 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (NCH <= 4) ? DS_WARP_MINB 
     int cnt = (int)((ca - col0) >> 8);
     int ctot = warp_sum_i(cnt);
 
-    // ---- step 3: the guess must cover the top k; otherwise keep every finite element
-    if (guessed && ctot < k) {
-      tlo = -FLT_MAX;
+    // ---- step 3: the guess must cover the top k. Otherwise lower it once by
+    // 0.3 sd (a few dozen more candidates near the usual quantiles), and if that
+    // still falls short keep every finite element: a short count is usually a
+    // near miss, and keeping all V elements costs several cells' work.
+#pragma unroll 1
+    for (int retry = 0; guessed && ctot < k && retry < 2; ++retry) {
+      const float lower = tlo - 0.3f * sd;
+      tlo = (retry == 0 && lower < tlo && lower > -FLT_MAX) ? lower : -FLT_MAX;
       ca = col0;
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {

@@ -1,13 +1,19 @@
 /*
  * dsample.h -- C ABI of libdsample, the GB300 (sm_103a) vocab-wide sampling pass.
  *
- * Two calls, both asynchronous on the caller's CUDA stream, both allocating
- * nothing and keeping no state between calls:
+ * The two hot-path calls:
  *
  *   ds_sample      classifier-free-guidance combine, full-vocab max / logsumexp,
  *                  exact top-ratio filter and Gumbel-max sampling at per-request
  *                  temperature; one (token, logprob) per (row, position) cell.
  *   ds_greedy_lse  per-row max, logsumexp and argmax over a large vocabulary.
+ *
+ * and the calls around them: ds_sample_ex (per-request ratios and iterations,
+ * keep-ties mode), ds_reveal (confidence ranking and reveal), ds_merge_triples
+ * (vocabulary-shard merge) and ds_log_softmax (dense log-probabilities). All are
+ * asynchronous on the caller's CUDA stream, allocate nothing and keep no state
+ * between calls beyond a process-wide count of kernel launches
+ * (ds_launch_count).
  *
  * All pointers named "device" must be CUDA device (or managed) memory of the
  * current device; the library never frees or retains them. Inputs are never

@@ -33,8 +33,13 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["ds_device.cuh", "ds_sample_common.cuh", "k_sample_warp.cu", "k_sample_cluster.cu",
-                  "k_sample_stream.cu", "k_greedy.cu", "ds_api.cu"]
+# The sources that define each workload's kernels and their launch plan: its
+# committed DRAM figure stays valid while their code is unchanged.
+KERNEL_SOURCES = {
+    "cfg3": ["ds_device.cuh", "ds_sample_common.cuh", "k_sample_warp.cu"],
+    "cfg5": ["ds_device.cuh", "ds_sample_common.cuh", "k_sample_stream.cu", "k_sample_cluster.cu"],
+    "cfg4": ["ds_device.cuh", "k_greedy.cu"],
+}
 
 
 # ------------------------------------------------------------------------------------- helpers
@@ -58,11 +63,11 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
-    """Hash of the kernel sources' code: line comments and trailing blanks are dropped, so
-    that an edited comment does not retire the committed traffic figures."""
+def kernel_source_hash(workload):
+    """Hash of the code of a workload's kernel sources: line comments and trailing blanks are
+    dropped, so that an edited comment does not retire the committed traffic figures."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[workload]:
         with open(os.path.join(ROOT, "vocab_wide_logit_gb300", "csrc", name), encoding="utf-8") as f:
             for line in f:
                 code = line.split("//", 1)[0].rstrip()
@@ -80,7 +85,7 @@ def committed_traffic(workload):
     except (OSError, ValueError):
         return None
     e = d.get(workload)
-    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+    if not e or e.get("kernel_source_hash") != kernel_source_hash(workload):
         return None
     return e.get("dram_bytes_per_launch")
 

@@ -31,17 +31,20 @@ double normal_upper_quantile(double p) {
   return 0.5 * (lo + hi);
 }
 
+// SM count of the current device, cached per device (callers on several host
+// threads may race to fill an entry; they store the same value).
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  static int cached_dev = -1, cached_sms = 0;
-  if (dev != cached_dev) {
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    cached_dev = dev;
-    cached_sms = sms;
+  static std::atomic<int> cache[64];
+  if (dev >= 0 && dev < 64) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
   }
-  return cached_sms;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) cache[dev].store(sms, std::memory_order_relaxed);
+  return sms;
 }
 
 std::atomic<unsigned long long> g_launches{0};

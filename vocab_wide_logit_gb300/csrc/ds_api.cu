@@ -197,12 +197,16 @@ ds_status ds_log_softmax(const void* logits, int32_t n, int32_t V, void* out, in
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const uint16_t* x = static_cast<const uint16_t*>(logits);
   const bool bf16_out = out_dtype == DS_DTYPE_BF16;
-  cudaError_t e;
+  cudaError_t e = cudaErrorLaunchOutOfResources;
   if (ds::log_softmax_fused_fits(V)) {
-    // the row held on chip by a cluster: one read of the logits
+    // the row held on chip by a cluster: one read of the logits (out of resources
+    // means no cluster of that shape fits this device, and nothing was launched)
     e = ds::launch_log_softmax_fused(x, n, V, out_max, out_lse, out_argmax, out, bf16_out, st);
-  } else {
-    // the triple pass, then the write pass (a second read of the logits)
+  }
+  if (e == cudaErrorLaunchOutOfResources) {
+    // the triple pass, then the write pass (a second read of the logits); the
+    // refused configuration's error is cleared first
+    (void)cudaGetLastError();
     e = ds::launch_greedy(x, n, V, out_max, out_lse, out_argmax, st);
     if (e == cudaSuccess) e = ds::launch_log_softmax_write(x, n, V, out_lse, out, bf16_out, st);
   }

@@ -54,8 +54,9 @@ typedef enum {
  * Defined by: "Sampler support for discrete diffusion" (mstar issue #267),
  * Hert4's first comment (log-softmax, argmax and confidence per cell; logits
  * [C, T, V] with T ragged across requests; CFG combine of two logit tensors;
- * top-ratio filter keeping ceil(0.1 * V); Gumbel sampling; "sample every
- * position handed in, return (tokens, logprobs)"), and "Add a sampler resource
+ * top-ratio filter keeping ceil(0.1 * V); Gumbel sampling; the sampler returns
+ * a (token, logprob) for every position it is given and leaves ranking to the
+ * caller), and "Add a sampler resource
  * for discrete diffusion" (mstar PR #290), Contract (sample(request_ids,
  * c_logits, u_logits, seq_lens, iterations) over [rows, positions, vocab]
  * packed across requests; per-request guidance and temperature; no
@@ -122,14 +123,24 @@ ds_status ds_sample(const int32_t* request_ids, const void* c_logits, const void
  *   iterations   device uint32 [B] or NULL. When given, request r's noise uses
  *                iterations[r] (< 2^24, else as an invalid ratio) and iteration
  *                is ignored.
- *   flags        0, or DS_FLAG_KEEP_TIES: the kept set becomes every id whose z
+ *   flags        OR of:
+ *                DS_FLAG_KEEP_TIES: the kept set becomes every id whose z
  *                reaches the k-th largest z, so ids tied with the k-th are kept
- *                too (the pages' "keep the ceil(0.1 V) largest" leaves ties at
- *                the cut open; by default exactly k are kept, smallest ids first).
+ *                too (the pages keep the ceil(0.1 V) largest logits but do not
+ *                say which of several tied at the cut; by default exactly k are
+ *                kept, smallest ids first).
+ *                DS_FLAG_SKIP_EXACT_PASS (diagnostic): the fast pass runs alone;
+ *                a cell it cannot settle exactly is left with token
+ *                DS_MARKED_TOKEN and an unspecified logprob instead of being
+ *                finished by the exact pass that normally follows it on the
+ *                stream. Every other cell is as without the flag. This lets a
+ *                caller (a test, a profiler) count how often the exact pass runs.
  * With both arrays NULL and flags 0 this is ds_sample. Per-request arrays must
  * be 4-byte aligned. Unknown flag bits: DS_ERR_INVALID_ARG. Returns as ds_sample.
  */
 #define DS_FLAG_KEEP_TIES 1u
+#define DS_FLAG_SKIP_EXACT_PASS 2u
+#define DS_MARKED_TOKEN (-2)
 ds_status ds_sample_ex(const int32_t* request_ids, const void* c_logits, const void* u_logits,
                        const int32_t* seq_lens, int32_t B, int32_t C, int32_t P, int32_t V,
                        const float* guidance, const float* temperature, const float* top_ratios,

@@ -12,8 +12,8 @@
  *    first comment: log-softmax, argmax and max log-prob per cell; logits
  *    [C, T, V] with T ragged across requests; classifier-free-guidance combine
  *    of two logit tensors; top-ratio filter keeping ceil(0.1 * V) tokens;
- *    Gumbel sampling; "sample every position handed in, return (tokens,
- *    logprobs)".
+ *    Gumbel sampling; a (token, logprob) is returned for every position the
+ *    sampler is given, and ranking is left to the caller.
  *  - "Add a sampler resource for discrete diffusion" (mstar PR #290),
  *    "Contract": sample(request_ids, c_logits, u_logits, seq_lens, iterations)
  *    over [rows, positions, vocab] packed across requests; per-request guidance

@@ -132,5 +132,5 @@ def test_sample_ex_argument_errors(lib):
     assert ex(ratios=ctypes.c_void_p(0x100002), ratio=0.0) == _lib.DS_ERR_INVALID_ARG  # misaligned array
     assert ex(iters=ctypes.c_void_p(0x100001), it=1 << 24) == _lib.DS_ERR_INVALID_ARG
     assert ex(V=_lib.DS_MAX_VOCAB + 1) == _lib.DS_ERR_UNSUPPORTED
-    assert ex(flags=2) == _lib.DS_ERR_INVALID_ARG
+    assert ex(flags=4) == _lib.DS_ERR_INVALID_ARG
     assert lib.ds_sample_ex(f, f, None, f, 1, 0, 1, 8, f, f, None, 0.1, 0, None, 0, 1, f, f, None, None) == _lib.DS_OK

@@ -5,6 +5,11 @@ within 1e-5 relative of each other; those near-ties are counted and reported, no
 Bar (logprob, lse): |delta| <= 1e-4 absolute (fp32 accumulation on the GPU, double in the oracle).
 Bar (max, argmax, temperature-0 tokens): bit-exact.
 """
+import concurrent.futures
+import json
+import os
+import platform
+
 import numpy as np
 import pytest
 import torch
@@ -17,6 +22,34 @@ pytestmark = pytest.mark.gpu
 
 LOGPROB_TOL = 1e-4
 NEAR_TIE_REL = 1e-5
+
+# Per-workload parity statistics of this run; written as JSON to $DS_PARITY_OUT (when set) once the
+# module's tests are done, so that the counts the near-tie exemption used are kept, not just printed.
+PARITY = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _parity_report():
+    yield
+    path = os.environ.get("DS_PARITY_OUT")
+    if path and PARITY:
+        doc = {"bar": {"tokens": "bit-exact except near-ties |s1 - s2| < 1e-5 max(|s1|, 1) (oracle scores)",
+                       "logprob": "|delta| <= %g" % LOGPROB_TOL},
+               "device": torch.cuda.get_device_name(0) if torch.cuda.is_available() else None,
+               "torch": torch.__version__, "host": platform.machine(), "workloads": PARITY}
+        with open(path, "w") as f:
+            json.dump(doc, f, indent=1, sort_keys=True)
+
+
+def _record(key, st, **extra):
+    agg = PARITY.setdefault(key, {"cells": 0, "near_ties": 0, "near_tie_mismatches": 0, "max_dlogprob": 0.0,
+                                  "calls": 0})
+    agg["cells"] += st["cells"]
+    agg["near_ties"] += st["near_ties"]
+    agg["near_tie_mismatches"] += st["near_tie_mismatches"]
+    agg["max_dlogprob"] = max(agg["max_dlogprob"], st["max_dlogprob"])
+    agg["calls"] += 1
+    agg.update(extra)
 
 
 def _dev():
@@ -39,22 +72,37 @@ class Dev:
         self.u = inp.u_logits.to(dev) if inp.u_logits is not None else None
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def run(self, seed, iteration, c=None, u="same"):
+    def run(self, seed, iteration, c=None, u="same", flags=0):
         c = self.c if c is None else c
         u = self.u if isinstance(u, str) else u
         tok = torch.full((self.inp.C, self.inp.P), -7, dtype=torch.int32, device=c.device)
         lp = torch.full((self.inp.C, self.inp.P), 7.0, dtype=torch.float32, device=c.device)
         pkg.ds_sample(self.rid, c, u, self.sl, self.g, self.tau, self.inp.top_ratio, seed, iteration, tok, lp,
-                      d_status=self.status, B=self.inp.B, C=self.inp.C, P=self.inp.P, V=self.inp.V)
+                      d_status=self.status, B=self.inp.B, C=self.inp.C, P=self.inp.P, V=self.inp.V, flags=flags)
         torch.cuda.synchronize()
         return tok.cpu().numpy().reshape(-1), lp.cpu().numpy().reshape(-1)
 
 
-def oracle_cells(inp, seed, iteration, cells=None):
-    return oracle.sample_cells(inp.request_ids, wl.bf16_bits(inp.c_logits),
-                               wl.bf16_bits(inp.u_logits) if inp.u_logits is not None else None,
-                               inp.seq_lens, inp.C, inp.P, inp.V, inp.guidance, inp.temperature,
-                               inp.top_ratio, seed, iteration, cells)
+def oracle_cells(inp, seed, iteration, cells=None, bits=None):
+    """The oracle on the listed cells (all when None). The oracle is single-threaded C++ and its
+    ctypes call releases the GIL, so large cell lists are split over host threads."""
+    cb, ub = bits if bits is not None else _bits(inp)
+    if cells is None:
+        cells = np.arange(inp.C * inp.P, dtype=np.int64)
+    cells = np.asarray(cells, dtype=np.int64)
+    run = lambda cs: oracle.sample_cells(inp.request_ids, cb, ub, inp.seq_lens, inp.C, inp.P, inp.V,
+                                         inp.guidance, inp.temperature, inp.top_ratio, seed, iteration, cs)
+    workers = min(os.cpu_count() or 1, 16)
+    if workers <= 1 or inp.V * len(cells) < 4_000_000:
+        return run(cells)
+    parts = np.array_split(cells, workers * 4)
+    with concurrent.futures.ThreadPoolExecutor(workers) as ex:
+        outs = list(ex.map(run, parts))
+    return {k: np.concatenate([o[k] for o in outs]) for k in outs[0]}
+
+
+def _bits(inp):
+    return (wl.bf16_bits(inp.c_logits), wl.bf16_bits(inp.u_logits) if inp.u_logits is not None else None)
 
 
 def compare(inp, got_tok, got_lp, ref, cells=None, max_near_frac=0.01, label=""):
@@ -62,8 +110,9 @@ def compare(inp, got_tok, got_lp, ref, cells=None, max_near_frac=0.01, label="")
         cells = np.arange(inp.C * inp.P)
     gt = got_tok[cells]
     gl = got_lp[cells]
-    gap = ref["top1"] - ref["top2"]
-    near = np.abs(gap) < NEAR_TIE_REL * np.maximum(np.abs(ref["top1"]), 1.0)
+    with np.errstate(invalid="ignore"):
+        gap = ref["top1"] - ref["top2"]
+        near = np.abs(gap) < NEAR_TIE_REL * np.maximum(np.abs(ref["top1"]), 1.0)
     match = gt == ref["tokens"]
     bad = ~match & ~near
     if bad.any():
@@ -92,7 +141,7 @@ def test_config1_all_cells():
     ref = oracle_cells(inp, inp.seed, 0)
     st = compare(inp, tok, lp, ref, label="cfg1")
     assert int(d.status.item()) == 0
-    print("cfg1", st)
+    _record("cfg1", st, iterations=[0])
 
 
 def test_config2_mixed_guidance_and_temperature():
@@ -105,30 +154,29 @@ def test_config2_mixed_guidance_and_temperature():
         tok, lp = d.run(inp.seed, it)
         ref = oracle_cells(inp, inp.seed, it)
         st = compare(inp, tok, lp, ref, label="cfg2 it%d" % it)
+        _record("cfg2", st, iterations=[0, 1, 5])
         # greedy requests: exact argmax everywhere
         greedy_rows = np.repeat(inp.temperature == 0, inp.seq_lens)
         gmask = np.tile(greedy_rows, inp.C)
         assert np.array_equal(tok[gmask], ref["tokens"][gmask])
     assert int(d.status.item()) == 0
-    print("cfg2", st)
 
 
-def test_config3_full_batch_sampled_cells():
-    """Full-size launch (as the benchmark times it); the oracle checks 3000 sampled cells
-    on each of four of the 32 iterations."""
+def test_config3_every_cell_of_every_iteration():
+    """Full-size launch, as the benchmark times it (every iteration 0..31 of the same buffers), with
+    every one of the 124080 cells of every iteration checked against the oracle."""
     dev = _dev()
     inp = wl.config3()
     d = Dev(inp, dev)
-    rng = np.random.Generator(np.random.PCG64(33))
-    for it in (0, 1, 17, 31):
+    bits = _bits(inp)
+    for it in range(32):
         tok, lp = d.run(inp.seed, it)
-        cells = np.sort(rng.choice(inp.C * inp.P, size=3000, replace=False))
-        ref = oracle_cells(inp, inp.seed, it, cells)
-        st = compare(inp, tok, lp, ref, cells, label="cfg3 it%d" % it)
+        ref = oracle_cells(inp, inp.seed, it, bits=bits)
+        st = compare(inp, tok, lp, ref, label="cfg3 it%d" % it)
+        _record("cfg3", st, iterations="0..31")
         assert (tok >= 0).all() and (tok < inp.V).all()
         assert np.all(lp <= 1e-6)
     assert int(d.status.item()) == 0
-    print("cfg3", st)
 
 
 def test_config4_greedy_large_vocab():
@@ -146,19 +194,31 @@ def test_config4_greedy_large_vocab():
     p = np.exp(mx.cpu().numpy().astype(np.float64) - lse.cpu().numpy())
     p_ref = np.exp(ref["max"].astype(np.float64) - ref["lse"])
     assert np.max(np.abs(p - p_ref) / p_ref) <= 2e-4
+    PARITY["cfg4"] = {"rows": g.n, "max_exact": True, "argmax_exact": True,
+                      "planted_tie_rows": len(g.planted_rows),
+                      "max_dlse": float(np.max(np.abs(lse.cpu().numpy() - ref["lse"]))),
+                      "max_rel_dp": float(np.max(np.abs(p - p_ref) / p_ref))}
 
 
-def test_config5_large_vocab_sampled_cells():
+def test_config5_every_cell():
+    """Full-size large-vocabulary launch (the benchmark's launch plan: single CTAs, then pairs for
+    the last cells, then the exact pass over marked cells): every one of the 1024 cells at
+    iterations 0, 1 and 31. The cells the streaming pass leaves to the exact pass are counted with
+    the diagnostic flag that skips that pass."""
     dev = _dev()
     inp = wl.config5()
     d = Dev(inp, dev)
-    tok, lp = d.run(inp.seed, 0)
-    rng = np.random.Generator(np.random.PCG64(55))
-    cells = np.sort(rng.choice(inp.C * inp.P, size=96, replace=False))
-    ref = oracle_cells(inp, inp.seed, 0, cells)
-    st = compare(inp, tok, lp, ref, cells, label="cfg5")
+    bits = _bits(inp)
+    marked = 0
+    for it in (0, 1, 31):
+        tok, lp = d.run(inp.seed, it)
+        ref = oracle_cells(inp, inp.seed, it, bits=bits)
+        st = compare(inp, tok, lp, ref, label="cfg5 it%d" % it)
+        mt, _ = d.run(inp.seed, it, flags=pkg.DS_FLAG_SKIP_EXACT_PASS)
+        marked += int((mt == pkg.DS_MARKED).sum())
+        assert np.array_equal(mt[mt != pkg.DS_MARKED], tok[mt != pkg.DS_MARKED])
+        _record("cfg5", st, iterations=[0, 1, 31], cells_left_to_exact_pass=marked)
     assert int(d.status.item()) == 0
-    print("cfg5", st)
 
 
 # ------------------------------------------------------------------------------------------ edge grids
@@ -251,6 +311,28 @@ def test_misaligned_rows_and_u_alignment_differing_from_c():
         compare(inp, tok, lp, oracle_cells(inp, 8, 2), label="misaligned V=%d c+%d u+%d" % (V, c_off, u_off))
 
 
+@pytest.mark.parametrize("V", [2048, 2055, 2056])
+def test_warp_to_stream_switch_with_misaligned_rows(V):
+    """Both sides of the switch from the one-warp-per-cell kernel (V <= 2055, where a lane holds
+    the most chunks and the longest scalar head or tail) to the streaming kernel (V >= 2056), with
+    c and u rows starting at odd 2-byte offsets that differ between c and u."""
+    dev = _dev()
+    inp = wl.make_sample_inputs("sw%d" % V, C=2, seq_lens=[3, 5, 2], V=V, guidance=[2.0, 0.0, 1.5],
+                                temperature=[0.9, 1.4, 0.0], sigma_c=3.0, sigma_u=1.5, top_ratio=0.1, seed=V)
+    d = Dev(inp, dev)
+    for c_off, u_off in ((0, 0), (1, 6), (3, 0)):
+        cbuf = torch.zeros(inp.c_logits.numel() + 8, dtype=torch.bfloat16, device=dev)
+        cbuf[c_off:c_off + inp.c_logits.numel()] = d.c.reshape(-1)
+        ubuf = torch.zeros(inp.u_logits.numel() + 8, dtype=torch.bfloat16, device=dev)
+        ubuf[u_off:u_off + inp.u_logits.numel()] = d.u.reshape(-1)
+        c_view = cbuf[c_off:c_off + inp.c_logits.numel()].view(inp.C, inp.P, V)
+        u_view = ubuf[u_off:u_off + inp.u_logits.numel()].view(inp.C, inp.P_u, V)
+        for it in (0, 5):
+            tok, lp = d.run(19, it, c=c_view, u=u_view)
+            compare(inp, tok, lp, oracle_cells(inp, 19, it), label="V=%d c+%d u+%d it%d" % (V, c_off, u_off, it))
+    assert int(d.status.item()) == 0
+
+
 def test_neg_inf_logits():
     dev = _dev()
     for V in (1025, 9000):
@@ -339,9 +421,16 @@ def test_large_vocab_hot_temperatures_take_the_exact_path():
     inp = wl.make_sample_inputs("hot", C=1, seq_lens=[3, 3, 2], V=131072, guidance=[1.0, 0.0, 2.0],
                                 temperature=[4.0, 0.7, 9.0], sigma_c=1.0, sigma_u=0.5, top_ratio=0.05, seed=8)
     d = Dev(inp, dev)
+    marked = 0
     for it in (0, 1):
         tok, lp = d.run(31, it)
         compare(inp, tok, lp, oracle_cells(inp, 31, it), label="hot it%d" % it)
+        mt, _ = d.run(31, it, flags=pkg.DS_FLAG_SKIP_EXACT_PASS)
+        marked += int((mt == pkg.DS_MARKED).sum())
+        assert np.array_equal(mt[mt != pkg.DS_MARKED], tok[mt != pkg.DS_MARKED])
+    # the exact pass did run on some cells here, and its results are the ones compared above
+    assert marked > 0
+    PARITY["hot_temperatures_v131072"] = {"cells": 2 * inp.cells, "cells_left_to_exact_pass": marked}
     assert int(d.status.item()) == 0
 
 

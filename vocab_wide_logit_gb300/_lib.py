@@ -23,6 +23,8 @@ DS_MAX_VOCAB = 262137
 EXPORTED = ("ds_sample", "ds_greedy_lse", "ds_status_string", "ds_top_k", "ds_merge_triples", "ds_log_softmax",
             "ds_reveal", "ds_sample_ex", "ds_launch_count")
 DS_FLAG_KEEP_TIES = 1
+DS_FLAG_SKIP_EXACT_PASS = 2
+DS_MARKED = -2
 DS_DTYPE_F32 = 0
 DS_DTYPE_BF16 = 1
 
@@ -94,17 +96,19 @@ def _stream(stream):
 
 def ds_sample(request_ids, c_logits, u_logits, seq_lens, guidance, temperature, top_ratio, seed,
               iteration, out_tokens, out_logprobs, d_status=None, B=None, C=None, P=None, V=None,
-              stream=None, check=True, top_ratios=None, iterations=None, keep_ties=False):
+              stream=None, check=True, top_ratios=None, iterations=None, keep_ties=False, flags=0):
     """Call ds_sample (ds_sample_ex when per-request top_ratios / iterations are given) on device
     tensors. Shapes: c_logits [C, P, V] bf16, u_logits [C, P_u, V] bf16 or None,
     request_ids/seq_lens int32 [B], guidance/temperature float32 [B], top_ratios float32 [B] or
     None, iterations int32/uint32 [B] or None, out_tokens int32 [C, P], out_logprobs float32
-    [C, P], d_status uint32/int32 [1] or None."""
+    [C, P], d_status uint32/int32 [1] or None. flags: extra DS_FLAG_* bits (keep_ties sets
+    DS_FLAG_KEEP_TIES)."""
     if C is None:
         C, P, V = c_logits.shape
     if B is None:
         B = seq_lens.shape[0]
-    if top_ratios is None and iterations is None and not keep_ties:
+    flags = int(flags) | (DS_FLAG_KEEP_TIES if keep_ties else 0)
+    if top_ratios is None and iterations is None and flags == 0:
         rc = load().ds_sample(_ptr(request_ids), _ptr(c_logits), _ptr(u_logits), _ptr(seq_lens), int(B),
                               int(C), int(P), int(V), _ptr(guidance), _ptr(temperature), float(top_ratio),
                               int(seed) & (2 ** 64 - 1), int(iteration), _ptr(out_tokens), _ptr(out_logprobs),
@@ -114,7 +118,7 @@ def ds_sample(request_ids, c_logits, u_logits, seq_lens, guidance, temperature, 
         rc = load().ds_sample_ex(_ptr(request_ids), _ptr(c_logits), _ptr(u_logits), _ptr(seq_lens), int(B),
                                  int(C), int(P), int(V), _ptr(guidance), _ptr(temperature), _ptr(top_ratios),
                                  float(top_ratio), int(seed) & (2 ** 64 - 1), _ptr(iterations), int(iteration),
-                                 DS_FLAG_KEEP_TIES if keep_ties else 0, _ptr(out_tokens), _ptr(out_logprobs),
+                                 flags, _ptr(out_tokens), _ptr(out_logprobs),
                                  _ptr(d_status), _stream(stream))
         name = "ds_sample_ex"
     if check and rc != DS_OK:

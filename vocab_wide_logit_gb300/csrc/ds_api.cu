@@ -85,7 +85,7 @@ ds_status ds_sample_ex(const int32_t* request_ids, const void* c_logits, const v
                        uint32_t flags, int32_t* out_tokens, float* out_logprobs, uint32_t* d_status,
                        void* stream) {
   if (B < 0 || C < 0 || P < 0 || V < 1) return DS_ERR_INVALID_ARG;
-  if ((flags & ~(uint32_t)DS_FLAG_KEEP_TIES) != 0u) return DS_ERR_INVALID_ARG;
+  if ((flags & ~(uint32_t)(DS_FLAG_KEEP_TIES | DS_FLAG_SKIP_EXACT_PASS)) != 0u) return DS_ERR_INVALID_ARG;
   if (C > DS_MAX_ROWS) return DS_ERR_INVALID_ARG;
   if (!iterations && iteration > DS_MAX_ITERATION) return DS_ERR_INVALID_ARG;
   if (!top_ratios && !(top_ratio > 0.0f && top_ratio <= 1.0f)) return DS_ERR_INVALID_ARG;
@@ -147,7 +147,7 @@ ds_status ds_sample_ex(const int32_t* request_ids, const void* c_logits, const v
     // finished by the staged kernel right behind it on the same stream (with
     // per-request ratios every k is possible, and this pair handles each)
     e = ds::launch_sample_stream(a, st);
-    if (e == cudaSuccess) e = ds::launch_sample_cluster(a, st, 1);
+    if (e == cudaSuccess && !(flags & DS_FLAG_SKIP_EXACT_PASS)) e = ds::launch_sample_cluster(a, st, 1);
   } else {
     e = ds::launch_sample_cluster(a, st, 0);
   }
@@ -197,16 +197,15 @@ ds_status ds_log_softmax(const void* logits, int32_t n, int32_t V, void* out, in
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const uint16_t* x = static_cast<const uint16_t*>(logits);
   const bool bf16_out = out_dtype == DS_DTYPE_BF16;
-  cudaError_t e = cudaErrorLaunchOutOfResources;
-  if (ds::log_softmax_fused_fits(V)) {
-    // the row held on chip by a cluster: one read of the logits (out of resources
-    // means no cluster of that shape fits this device, and nothing was launched)
-    e = ds::launch_log_softmax_fused(x, n, V, out_max, out_lse, out_argmax, out, bf16_out, st);
+  cudaError_t e = cudaSuccess;
+  bool two_pass = !ds::log_softmax_fused_fits(V);
+  if (!two_pass) {
+    // the row held on chip by a cluster: one read of the logits; refused (nothing
+    // launched) when no cluster of that shape fits this device
+    e = ds::launch_log_softmax_fused(x, n, V, out_max, out_lse, out_argmax, out, bf16_out, st, &two_pass);
   }
-  if (e == cudaErrorLaunchOutOfResources) {
-    // the triple pass, then the write pass (a second read of the logits); the
-    // refused configuration's error is cleared first
-    (void)cudaGetLastError();
+  if (e == cudaSuccess && two_pass) {
+    // the triple pass, then the write pass (a second read of the logits)
     e = ds::launch_greedy(x, n, V, out_max, out_lse, out_argmax, st);
     if (e == cudaSuccess) e = ds::launch_log_softmax_write(x, n, V, out_lse, out, bf16_out, st);
   }

@@ -12,7 +12,7 @@ namespace ds {
 void note_launch();
 
 constexpr int kWarpKernelThreads = 128;
-constexpr int kStreamMark = -2;  // out_tokens marker left by the streaming kernel for the staged one
+constexpr int kStreamMark = DS_MARKED_TOKEN;  // out_tokens marker left by a fast pass for the exact one
 
 // Largest V of the one-warp-per-cell kernel and of the cluster kernel.
 int warp_kernel_max_vocab();
@@ -35,9 +35,11 @@ cudaError_t launch_log_softmax_write(const uint16_t* x, int n, int V, const floa
                                      cudaStream_t st);
 
 // Dense log-softmax with each row held in a cluster's shared memory (one read of
-// the logits); fits when a row splits into at most 8 slices of 64 KB.
+// the logits); fits when a row splits into at most 8 slices of 64 KB. When no
+// cluster of the needed shape fits the device, *refused is set, nothing is
+// launched and cudaSuccess is returned.
 bool log_softmax_fused_fits(int V);
 cudaError_t launch_log_softmax_fused(const uint16_t* x, int n, int V, float* out_max, float* out_lse,
-                                     int* out_argmax, void* out, bool bf16_out, cudaStream_t st);
+                                     int* out_argmax, void* out, bool bf16_out, cudaStream_t st, bool* refused);
 
 }  // namespace ds

@@ -287,7 +287,8 @@ bool log_softmax_fused_fits(int V) {
 }
 
 cudaError_t launch_log_softmax_fused(const uint16_t* x, int n, int V, float* out_max, float* out_lse,
-                                     int* out_argmax, void* out, bool bf16_out, cudaStream_t st) {
+                                     int* out_argmax, void* out, bool bf16_out, cudaStream_t st, bool* refused) {
+  *refused = false;
   if (n <= 0) return cudaSuccess;
   // the fewest CTAs per row whose slices fit (shared memory per CTA = one slice)
   const long long nq = ((long long)V + 14) >> 3;
@@ -312,17 +313,23 @@ cudaError_t launch_log_softmax_fused(const uint16_t* x, int n, int V, float* out
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   cfg.gridDim = dim3((unsigned)cs, 1, 1);
+  // No cluster of this shape fits the device (the query fails or finds none):
+  // refuse before launching anything, so the caller can take the two-pass form.
+  // Only the query's own error is cleared here.
   int max_clusters = 0;
   e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-  if (e != cudaSuccess) return e;
-  if (max_clusters < 1) return cudaErrorLaunchOutOfResources;
+  if (e != cudaSuccess) (void)cudaGetLastError();
+  if (e != cudaSuccess || max_clusters < 1) {
+    *refused = true;
+    return cudaSuccess;
+  }
   long long n_clusters = max_clusters;
   if (n_clusters > n) n_clusters = n;
   cfg.gridDim = dim3((unsigned)(n_clusters * cs), 1, 1);
   e = cudaLaunchKernelEx(&cfg, kern, x, n, V, out_max, out_lse, out_argmax, out);
   if (e != cudaSuccess) return e;
   note_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace ds

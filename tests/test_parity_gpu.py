@@ -92,6 +92,7 @@ def oracle_cells(inp, seed, iteration, cells=None, bits=None):
     cells = np.asarray(cells, dtype=np.int64)
     run = lambda cs: oracle.sample_cells(inp.request_ids, cb, ub, inp.seq_lens, inp.C, inp.P, inp.V,
                                          inp.guidance, inp.temperature, inp.top_ratio, seed, iteration, cs)
+    oracle.lib()  # build and load it once, before any thread calls it
     workers = min(os.cpu_count() or 1, 16)
     if workers <= 1 or inp.V * len(cells) < 4_000_000:
         return run(cells)

@@ -16,7 +16,7 @@ LIB = os.path.join(OUT, "libdsample.so")
 INCLUDE = os.path.join(ROOT, "include")
 SOURCES = ["ds_api.cu", "k_greedy.cu", "k_sample_warp.cu", "k_sample_cluster.cu", "k_sample_stream.cu",
            "k_merge.cu", "k_reveal.cu", "k_log_softmax.cu"]
-HEADERS = ["ds_device.cuh", "ds_sample_common.cuh", "ds_launch.h", "gen_gumbel_bounds.py"]
+HEADERS = ["ds_device.cuh", "ds_sample_common.cuh", "ds_warp_common.cuh", "ds_launch.h", "gen_gumbel_bounds.py"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

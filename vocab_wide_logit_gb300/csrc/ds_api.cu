@@ -141,7 +141,7 @@ ds_status ds_sample_ex(const int32_t* request_ids, const void* c_logits, const v
   if (V <= ds::warp_kernel_max_vocab()) {
     const int sms = device_sm_count();
     if (sms <= 0) return DS_ERR_CUDA;
-    e = ds::launch_sample_warp(a, st, sms);
+    e = ds::launch_sample_warp(a, st, sms, !(flags & DS_FLAG_SKIP_EXACT_PASS));
   } else if (top_ratios || 4LL * a.k <= (long long)V) {
     // streaming pass; the cells it cannot finish exactly are marked and
     // finished by the staged kernel right behind it on the same stream (with

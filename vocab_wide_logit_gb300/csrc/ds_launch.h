@@ -18,7 +18,11 @@ constexpr int kStreamMark = DS_MARKED_TOKEN;  // out_tokens marker left by a fas
 int warp_kernel_max_vocab();
 int cluster_kernel_max_vocab();
 
-cudaError_t launch_sample_warp(const SampleArgs& a, cudaStream_t st, int num_sms);
+// One warp per cell: a lean pass that marks the cells it cannot settle on its
+// common path (too few or too many candidates for its balanced list), then
+// (exact_pass) the full kernel over the marked cells only.
+cudaError_t launch_sample_warp(const SampleArgs& a, cudaStream_t st, int num_sms, bool exact_pass);
+
 // Staged cluster kernel (z kept in shared memory); with only_marked it finishes
 // just the cells the streaming kernel marked with kStreamMark.
 cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st, int only_marked);

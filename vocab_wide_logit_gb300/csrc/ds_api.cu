@@ -127,6 +127,11 @@ ds_status ds_sample_ex(const int32_t* request_ids, const void* c_logits, const v
   const double target_hi = kk - spread;
   a.q_lo = (target_lo >= (double)V) ? -INFINITY : (float)normal_upper_quantile(target_lo / (double)V);
   a.q_hi = (target_hi < 1.0) ? INFINITY : (float)normal_upper_quantile(target_hi / (double)V);
+  // The one-warp-per-cell kernel aims closer to k: its second guess is sized
+  // to the shortfall, so a short first count costs one more compaction pass
+  // while every candidate beyond 32 per lane costs a noise draw per lane.
+  const double target_w = kk + (std::sqrt(kk * (1.0 - kk / (double)V)) + 0.02 * kk + 2.0);
+  a.q_w = (target_w >= (double)V) ? -INFINITY : (float)normal_upper_quantile(target_w / (double)V);
   a.key0 = (uint32_t)(seed & 0xffffffffull);
   a.key1 = (uint32_t)(seed >> 32);
   a.iter_hi = iterations ? 0u : (iteration << 8);

@@ -29,6 +29,7 @@ struct SampleArgs {
   int32_t k;          // kept count
   float q_lo;         // N(0,1) quantile for the first lower threshold guess (-inf: keep all)
   float q_hi;         // N(0,1) quantile for the upper threshold (+inf: none)
+  float q_w;          // N(0,1) quantile of the one-warp-per-cell kernel's first guess
   uint32_t key0, key1;
   uint32_t iter_hi;   // iteration << 8
   uint32_t rk0[10], rk1[10];  // Philox round keys (key + r * Weyl constants), computed on the host

@@ -19,6 +19,7 @@ struct ReqCursor {
   uint32_t rid;
   int32_t k;         // kept count of the request
   float q_lo, q_hi;  // N(0,1) quantiles seeding the request's threshold guesses
+  float q_w;         // and the one-warp-per-cell kernel's first guess
   uint32_t iter_hi;  // the request's iteration << 8 (noise counter word 3)
   uint32_t perr;     // DS_DEV_ERR_PARAM when the request's ratio or iteration is invalid
 };
@@ -46,6 +47,7 @@ __device__ __forceinline__ void req_params(const SampleArgs& a, int r, ReqCursor
       cur.k = 1;
       cur.q_lo = -__builtin_huge_valf();
       cur.q_hi = __builtin_huge_valf();
+      cur.q_w = -__builtin_huge_valf();
     } else {
       int kk = (int)ceilf(ratio * (float)a.V);
       kk = kk < 1 ? 1 : (kk > a.V ? a.V : kk);
@@ -54,11 +56,14 @@ __device__ __forceinline__ void req_params(const SampleArgs& a, int r, ReqCursor
       const float spread = 1.5f * sqrtf(kf * (1.f - kf / Vf)) + 0.02f * kf + 4.f;
       cur.q_lo = (kf + spread >= Vf) ? -__builtin_huge_valf() : upper_quantile((kf + spread) / Vf);
       cur.q_hi = (kf - spread < 1.f) ? __builtin_huge_valf() : upper_quantile((kf - spread) / Vf);
+      const float tw = kf + sqrtf(kf * (1.f - kf / Vf)) + 0.02f * kf + 2.f;
+      cur.q_w = (tw >= Vf) ? -__builtin_huge_valf() : upper_quantile(tw / Vf);
     }
   } else {
     cur.k = a.k;
     cur.q_lo = a.q_lo;
     cur.q_hi = a.q_hi;
+    cur.q_w = a.q_w;
   }
   if (a.iters) {
     const uint32_t it = a.iters[r];

@@ -97,7 +97,7 @@ struct CellWalker {
     G.err = (!(G.tau >= 0.f) || isnan(G.g) || cur.perr) ? DS_DEV_ERR_PARAM
                                                         : ((G.g != 0.f && a.u == nullptr) ? DS_DEV_ERR_NO_UNCOND : 0u);
     G.k = cur.k;
-    G.q_lo = cur.q_lo;
+    G.q_lo = cur.q_w;
     G.iter_hi = cur.iter_hi;
     G.crow = a.c + cell * (long long)V;
     const uintptr_t ca = reinterpret_cast<uintptr_t>(G.crow);
@@ -275,7 +275,7 @@ __device__ __forceinline__ int rank_of(Get get, int n_it, float zw, int idw) {
 // scores, so a member is reached after at most ctot - k drops. Ranks come from
 // counting, so no shared-memory histogram (whose atomics serialise when the
 // keys share their top bytes) is needed.
-__device__ __forceinline__ float2 race_exact_by_rank(const SampleArgs& a, const float2* dense, float* score, int ctot,
+__device__ __noinline__ float2 race_exact_by_rank(const SampleArgs& a, const float2* dense, float* score, int ctot,
                                                      int k, float tau, uint32_t t32, uint32_t rid, uint32_t ctr3,
                                                      int lane) {
   const int n_it = (ctot + 31) >> 5;
@@ -320,6 +320,98 @@ __device__ __forceinline__ float2 race_exact_by_rank(const SampleArgs& a, const 
     if (warp_sum_i(c) < k) break;
     if (lane == 0) score[iw] = -kInf;
     __syncwarp();
+  }
+  return w;
+}
+
+// Exact G for the listed candidates of the balanced list (their indices in
+// list[0..n)), then the argmax by (score desc, id asc). Out of line: it runs
+// when the table bounds leave more than one candidate in reach.
+__device__ __noinline__ float2 race_listed(const SampleArgs& a, const float2* dense, const int* list, int n, float tau,
+                                          uint32_t t32, uint32_t rid, uint32_t ctr3, int lane) {
+  float bs = -kInf, bz = 0.f;
+  int bid = INT_MAX;
+  for (int o = lane; o < n; o += 32) {
+    const float2 v = dense[list[o]];
+    const int id = __float_as_int(v.y);
+    const uint32_t x = noise_word((uint32_t)id, t32, rid, ctr3, a.rk0, a.rk1);
+    const float scr = __fmaf_rn(tau, gumbel_accurate(x), v.x);
+    if (bid == INT_MAX || scr > bs || (scr == bs && id < bid)) {
+      bs = scr;
+      bid = id;
+      bz = v.x;
+    }
+  }
+  const int wl = warp_argmax_lane(bs, bid);
+  return make_float2(__shfl_sync(0xffffffffu, bz, wl), __int_as_float(__shfl_sync(0xffffffffu, bid, wl)));
+}
+
+// The race over a balanced candidate list of at most 32 NS candidates, with
+// the candidates lane + 32 q (q < NS) of each lane held in registers: every
+// draw, table bound and upper score stays in registers and the NS noise chains
+// run side by side. The winner is the one candidate whose upper score reaches
+// the best lower score S (less a margin); otherwise the candidates in reach get
+// exact G. A winner that ranks outside the top k takes the exact race.
+template <int NS>
+__device__ __forceinline__ float2 race_slots(const SampleArgs& a, const float2* dense, float* hs, int* list, int ctot,
+                                             int k, float tau, uint32_t t32, uint32_t rid, uint32_t ctr3, int lane) {
+  float2 v[NS];
+  uint32_t x[NS];
+  float lo[NS], hi[NS];
+#pragma unroll
+  for (int q = 0; q < NS; ++q) {
+    const int i = lane + 32 * q;
+    v[q] = dense[i];  // i < 256 = list capacity; entries past ctot are masked below
+    x[q] = noise_word(__float_as_uint(v[q].y), t32, rid, ctr3, a.rk0, a.rk1);
+  }
+  float lm = -kInf;
+#pragma unroll
+  for (int q = 0; q < NS; ++q) {
+    const bool ok = lane + 32 * q < ctot;
+    const float2 b = gumbel_bounds(x[q]);
+    lo[q] = ok ? __fmaf_rn(tau, b.x, v[q].x) : -kInf;
+    hi[q] = ok ? __fmaf_rn(tau, b.y, v[q].x) : -kInf;
+    lm = fmaxf(lm, lo[q]);
+  }
+  const float S = warp_max_r(lm);
+  const float thr = S - (fabsf(S) + 1.f) * 0x1p-20f;
+  int nin = 0;
+  float2 wv = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int q = 0; q < NS; ++q) {
+    const bool in = hi[q] >= thr;
+    nin += in ? 1 : 0;
+    wv = in ? v[q] : wv;
+  }
+  float2 w;
+  if (warp_sum_i(nin) == 1) {
+    const int src = __ffs(__ballot_sync(0xffffffffu, nin != 0)) - 1;
+    w = make_float2(__shfl_sync(0xffffffffu, wv.x, src), __shfl_sync(0xffffffffu, wv.y, src));
+  } else {
+    // exact G for the candidates still in reach (usually two or three), listed
+    // by their place in the balanced list
+    int n = 0;
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < NS; ++q) {
+      const bool in = hi[q] >= thr;
+      const unsigned b = __ballot_sync(0xffffffffu, in);
+      if (in) list[n + __popc(b & ((1u << lane) - 1u))] = lane + 32 * q;
+      n += __popc(b);
+    }
+    __syncwarp();
+    w = race_listed(a, dense, list, n, tau, t32, rid, ctr3, lane);
+  }
+  // membership of the winner in the exact top k: its rank among the candidates
+  if (ctot > k) {
+    const int idw = __float_as_int(w.y);
+    int c = 0;
+#pragma unroll
+    for (int q = 0; q < NS; ++q) {
+      const bool ok = lane + 32 * q < ctot;
+      c += (ok && (v[q].x > w.x || (!a.keep_ties && v[q].x == w.x && __float_as_int(v[q].y) < idw))) ? 1 : 0;
+    }
+    if (warp_sum_i(c) >= k) w = race_exact_by_rank(a, dense, hs, ctot, k, tau, t32, rid, ctr3, lane);
   }
   return w;
 }

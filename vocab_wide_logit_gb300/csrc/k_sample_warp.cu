@@ -292,11 +292,11 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (warp_min_blocks<NCH, FULL
           // ---- threshold guess from the subsample moments
           float tlo = -FLT_MAX;  // -FLT_MAX: keep every finite element
           bool guessed = false;
-          float sd = 0.f;
+          float sd = 0.f, mu = 0.f;
           if (NCH >= 2 && G.q_lo > -kInf) {
             const float inv_n = 1.0f / (float)(32 * 8 * (NCH > 1 ? NCH - 1 : 1));  // power of two: exact
             const float S1 = warp_sum(s1.x + s1.y), S2 = warp_sum(s2.x + s2.y);
-            const float mu = S1 * inv_n;
+            mu = S1 * inv_n;
             sd = sqrtf(fmaxf(fmaf(S2, inv_n, -mu * mu), 0.f));
             const float guess = fmaf(sd, G.q_lo, mu);
             if (isfinite(guess)) {
@@ -332,8 +332,16 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (warp_min_blocks<NCH, FULL
             cnt = (int)((ca - col0) >> 8);
             ctot = warp_sum_i(cnt);
             if (!guessed || ctot >= k || attempt == (FULL ? 2 : 1)) break;
-            const float lower = tlo - 0.3f * sd;
-            tlo = (attempt == 0 && lower < tlo && lower > -FLT_MAX) ? lower : -FLT_MAX;
+            // lower the threshold by the shortfall (and a dozen more) over the
+            // normal density at the first guess; the full kernel's third
+            // attempt keeps every finite element
+            float lower = -FLT_MAX;
+            if (attempt == 0 && sd > 0.f) {
+              const float qe = (tlo - mu) / sd;
+              const float dens = (float)a.V * 0.39894228f * __expf(-0.5f * qe * qe) / sd;
+              lower = tlo - (float)(k + 12 - ctot) / dens;
+            }
+            tlo = (lower < tlo && lower > -FLT_MAX) ? lower : -FLT_MAX;
           }
           __syncwarp();
           if (!FULL && (ctot < k || ctot > kDenseCap)) {
@@ -374,8 +382,19 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (warp_min_blocks<NCH, FULL
     // runs the exact select and race here, in both kernels: it is rare, and a
     // separate pass for it would cost more than its code)
     bool unsettled = false;
-    const float2 w = race_dense<true>(a, sm.dense, sm.r.hs, ctot, k, tau, (uint32_t)G.t, G.rid,
-                                      G.iter_hi | (uint32_t)G.c, lane, sm.r.hist, unsettled);
+    const uint32_t t32 = (uint32_t)G.t, ctr3 = G.iter_hi | (uint32_t)G.c;
+    float2 w;
+    // 97..160 candidates (the usual count near k = ceil(0.1 V) at V = 1025): the
+    // straight-line race over 4 or 5 candidates per lane; other counts: the
+    // loop over pairs. Only two straight-line variants are kept: each adds about
+    // 8 KB of code, and the kernel's hot code must stay within the SM's
+    // instruction cache.
+    switch ((ctot + 31) >> 5) {
+      case 4: w = race_slots<4>(a, sm.dense, sm.r.hs, sm.r.hist, ctot, k, tau, t32, G.rid, ctr3, lane); break;
+      case 5: w = race_slots<5>(a, sm.dense, sm.r.hs, sm.r.hist, ctot, k, tau, t32, G.rid, ctr3, lane); break;
+      default:
+        w = race_dense<true>(a, sm.dense, sm.r.hs, ctot, k, tau, t32, G.rid, ctr3, lane, sm.r.hist, unsettled);
+    }
     // ---- step 5: output (or, in the lean kernel, a mark for the exact pass)
     if (lane == 0) {
       if (unsettled) {

@@ -118,6 +118,9 @@ struct CellWalker {
 // Starts the copies of a cell's logits into the warp's shared buffers: each
 // lane copies its own chunks (lane + 32 j) to cdst(j) and udst(j), so it later
 // reads only what it copied. The scalar head or tail element goes to registers.
+// The kernel for NCH chunks per lane runs V >= 256 (NCH - 1) + 8, so a row
+// holds at least 32 (NCH - 1) full chunks at any alignment: chunks 0..NCH-2 of
+// every lane are always full and only the last is predicated.
 template <int NCH, typename CDst, typename UDst>
 __device__ __forceinline__ void prefetch_cell(const CellGeo& G, int lane, CDst cdst, UDst udst, uint32_t& sc,
                                               uint32_t& su) {
@@ -125,7 +128,10 @@ __device__ __forceinline__ void prefetch_cell(const CellGeo& G, int lane, CDst c
 #pragma unroll
   for (int j = 0; j < NCH; ++j) {
     const int q = lane + 32 * j;
-    cp_async16(cdst(j), (q < G.nfc) ? cb + q : cb, (q < G.nfc) ? 16u : 0u);
+    if (j < NCH - 1)
+      cp_async16(cdst(j), cb + q, 16u);
+    else
+      cp_async16(cdst(j), (q < G.nfc) ? cb + q : cb, (q < G.nfc) ? 16u : 0u);
   }
   sc = (lane < G.ns) ? (uint32_t)__ldg(G.crow + G.sid) : 0u;
   su = 0u;
@@ -135,7 +141,10 @@ __device__ __forceinline__ void prefetch_cell(const CellGeo& G, int lane, CDst c
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
         const int q = lane + 32 * j;
-        cp_async16(udst(j), (q < G.nfc) ? ub + q : ub, (q < G.nfc) ? 16u : 0u);
+        if (j < NCH - 1)
+          cp_async16(udst(j), ub + q, 16u);
+        else
+          cp_async16(udst(j), (q < G.nfc) ? ub + q : ub, (q < G.nfc) ? 16u : 0u);
       }
     } else {
       // u row aligned differently from the c row: gather element by element.

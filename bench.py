@@ -5,15 +5,24 @@ T ~ U{100..400} positions (P = 15510, 124080 cells), V = 1025, bf16 c and u,
 guidance 2, temperature 0.9, top ratio 0.1, seed 2. One step = one ds_sample call
 over the whole batch (iteration counter = step index mod 32). Inputs are 510 MB,
 far above the 129 MB L2, so no flush is needed between steps.
+
+Besides the contract's keys the line carries, for the headline and (under `also`)
+for every other configuration: the roofline of the call, the CPU oracle timed on
+a bounded sample of the same workload on this host, and parity statistics of the
+GPU output against the oracle on that sample (computed outside the timed region).
 `ms_per_call` adds the median and minimum of 64 single calls, each between its own
 pair of events, timed after the contract's region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload cfg3|cfg5|cfg4|cfg1|cfg2] [--no-extra]
 
-Under torchrun (N > 1) every rank runs its own full batch (weak scaling: cells are
-independent, no collective on the data path); the timed region is bracketed by
-barriers and the max over ranks is reported.
+With --gpus N > 1 outside torchrun the script starts N ranks itself (one process
+per GPU, torch.distributed.run on 127.0.0.1). Under torchrun every rank runs its
+own full batch (weak scaling: cells are independent, no collective on the data
+path); the timed region is bracketed by barriers and the max over ranks is
+reported. --launch-selftest runs the same launch, timing and reporting path on
+CPU ranks (gloo) with a sleep for a step, to check the multi-rank plumbing
+without a GPU; its line says so.
 """
 import argparse
 import hashlib
@@ -381,7 +390,7 @@ def dominant_kernel(w):
 
 def oracle_cpu_rate(inp, max_seconds=10.0, iteration=0):
     """Run the CPU oracle (single thread) on a bounded sample of the workload's cells.
-    Returns (cells per second, sample description, cells)."""
+    Returns (cells per second, sample description, cells, oracle outputs on those cells)."""
     import oracle
     from vocab_wide_logit_gb300 import workloads as wl
     cb = wl.bf16_bits(inp.c_logits)
@@ -394,12 +403,12 @@ def oracle_cpu_rate(inp, max_seconds=10.0, iteration=0):
                         inp.temperature, inp.top_ratio, inp.seed, iteration, cal)
     per = (time.perf_counter() - t0) / len(cal)
     want = int(min(n, max(len(cal), max_seconds / max(per, 1e-9))))
-    cells = np.linspace(0, n - 1, want).astype(np.int64)
+    cells = np.unique(np.linspace(0, n - 1, want).astype(np.int64))
     t0 = time.perf_counter()
-    oracle.sample_cells(inp.request_ids, cb, ub, inp.seq_lens, inp.C, inp.P, inp.V, inp.guidance,
-                        inp.temperature, inp.top_ratio, inp.seed, iteration, cells)
+    ref = oracle.sample_cells(inp.request_ids, cb, ub, inp.seq_lens, inp.C, inp.P, inp.V, inp.guidance,
+                              inp.temperature, inp.top_ratio, inp.seed, iteration, cells)
     dt = time.perf_counter() - t0
-    return want / dt, "%d of %d cells (evenly spaced), iteration %d" % (want, n, iteration), want
+    return len(cells) / dt, "%d of %d cells (evenly spaced), iteration %d" % (len(cells), n, iteration), cells, ref
 
 
 def oracle_cpu_rate_greedy(g, max_seconds=10.0):
@@ -412,33 +421,80 @@ def oracle_cpu_rate_greedy(g, max_seconds=10.0):
     want = int(min(g.n, max(1, max_seconds / max(per, 1e-9))))
     rows = np.arange(want, dtype=np.int64)
     t0 = time.perf_counter()
-    oracle.greedy_rows(bits, g.n, g.V, rows)
+    ref = oracle.greedy_rows(bits, g.n, g.V, rows)
     dt = time.perf_counter() - t0
-    return want / dt, "%d of %d rows" % (want, g.n), want
+    return want / dt, "%d of %d rows" % (want, g.n), rows, ref
+
+
+NEAR_TIE_REL = 1e-5
+
+
+def sample_parity(runner, iteration, cells, ref):
+    """GPU output of one call at `iteration` against the oracle on the sampled cells: tokens
+    bit-exact except near-ties (the two best perturbed scores, oracle side, within 1e-5 relative),
+    |delta logprob| on the matching cells."""
+    runner.step(iteration)
+    torch.cuda.synchronize()
+    tok = runner.tok.cpu().numpy().reshape(-1)[cells]
+    lp = runner.lp.cpu().numpy().reshape(-1)[cells].astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        near = np.abs(ref["top1"] - ref["top2"]) < NEAR_TIE_REL * np.maximum(np.abs(ref["top1"]), 1.0)
+    match = tok == ref["tokens"]
+    fin = match & np.isfinite(ref["logprobs"])
+    dl = np.abs(lp[fin] - ref["logprobs"][fin])
+    return {"cells": int(len(cells)), "token_mismatches": int((~match & ~near).sum()),
+            "near_ties": int(near.sum()), "near_tie_mismatches": int((~match & near).sum()),
+            "max_dlogprob": float(dl.max()) if dl.size else 0.0}
+
+
+def greedy_parity(runner, rows, ref):
+    runner.step(0)
+    torch.cuda.synchronize()
+    mx = runner.mx.cpu().numpy()[rows]
+    am = runner.am.cpu().numpy()[rows]
+    lse = runner.lse.cpu().numpy()[rows].astype(np.float64)
+    return {"rows": int(len(rows)), "max_mismatches": int((mx != ref["max"]).sum()),
+            "argmax_mismatches": int((am != ref["argmax"]).sum()),
+            "max_dlse": float(np.abs(lse - ref["lse"]).max())}
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu), for the baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return None
+
+
+def baseline_entry(value, unit, sample):
+    return {"value": round(value, 2), "unit": unit, "cores": 1, "kind": "oracle", "sample": sample,
+            "host_cpus": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def e2e_rate(inp, dev, steps):
     """Through the public API from pinned host memory: every step copies c (and u) host->device,
-    samples, and copies (tokens, logprobs) back."""
+    samples, and copies (tokens, logprobs) back; steps are pipelined two deep (the next step's copy
+    runs while this one samples). Host wall clock over K steps, device synchronised on both sides."""
     from vocab_wide_logit_gb300.api import HostSampler
     hs = HostSampler(torch.from_numpy(inp.request_ids), torch.from_numpy(inp.seq_lens.astype(np.int32)),
                      torch.from_numpy(inp.guidance), torch.from_numpy(inp.temperature), inp.C, inp.P, inp.P_u,
-                     inp.V, device=dev)
+                     inp.V, device=dev, depth=2)
     c_h = inp.c_logits.pin_memory()
     u_h = inp.u_logits.pin_memory() if inp.u_logits is not None else None
-    for i in range(2):
+    for i in range(3):
         hs(c_h, u_h, inp.top_ratio, inp.seed, i)
     torch.cuda.synchronize()
-    st = torch.cuda.current_stream()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for i in range(steps):
-        hs(c_h, u_h, inp.top_ratio, inp.seed, i % 32)
-    e1.record(st)
+    t0 = time.perf_counter()
+    slots = [hs.submit(c_h, u_h, inp.top_ratio, inp.seed, i % 32) for i in range(steps)]
+    for s in slots[-hs.depth:]:
+        hs.result(s)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    return inp.cells / (ms / 1e3), hs.h2d_bytes(), hs.d2h_bytes()
+    ms = (time.perf_counter() - t0) * 1e3 / steps
+    return inp.cells / (ms / 1e3), hs.h2d_bytes(), hs.d2h_bytes(), ms
 
 
 def roofline(bytes_per_step, ms, workload, kernel=None):
@@ -448,7 +504,8 @@ def roofline(bytes_per_step, ms, workload, kernel=None):
     ach = bytes_per_step / (ms / 1e3) / 1e9
     return {"bound": "hbm", "kernel": kernel, "achieved": round(ach, 1), "peak": peak, "peak_source": src,
             "unit": "GB/s", "frac": round(ach / peak, 4), "frac_of_8000": round(ach / 8000.0, 4),
-            "traffic": committed_traffic(workload), "algorithmic_bytes_per_launch": bytes_per_step}
+            "traffic": committed_traffic(workload) if workload in KERNEL_SOURCES else None,
+            "algorithmic_bytes_per_launch": bytes_per_step}
 
 
 def metric_name(is_greedy):
@@ -460,8 +517,32 @@ def run_config(w, is_greedy, world):
     """The workload description both arms report (the reference arm times the same workload)."""
     return {"workload": w.name, "units_per_gpu_step": w.n if is_greedy else w.cells,
             "bytes_per_gpu_step": w.algorithmic_bytes(),
-            "l2": "4 rotating input buffers, 508 MB total > L2" if is_greedy else "inputs larger than L2 (no flush)",
+            "l2": "4 rotating input buffers, 508 MB total > L2" if is_greedy else
+                  ("inputs larger than L2 (no flush)" if w.algorithmic_bytes() > 129e6 else
+                   "inputs smaller than L2 (a latency-bound call: L2-resident after the first step)"),
             "parallelism": "dp%d (independent cells per rank)" % world}
+
+
+def config_entry(name, dev, steps, warmup, cpu_seconds):
+    """Device time, roofline, the oracle timed on a bounded sample, and parity on that sample,
+    for one configuration (rank 0, N = 1)."""
+    w = make_workload(name)
+    is_greedy = name == "cfg4"
+    runner = GreedyRunner(w, dev) if is_greedy else SampleRunner(w, dev)
+    ms = time_steps(runner, steps, warmup, 1)
+    unit = "rows/s" if is_greedy else "sampled positions/s"
+    e = {"workload": w.name, "ms_per_step": round(ms, 5), "us_per_step": round(ms * 1e3, 2),
+         "ms_per_call": per_call_ms(runner, 64, warmup + steps),
+         "units_per_s": round(runner.units / (ms / 1e3), 1), "unit": unit,
+         "roofline": roofline(runner.bytes_per_step, ms, name, dominant_kernel(w))}
+    if is_greedy:
+        cv, sample, rows, ref = oracle_cpu_rate_greedy(w, cpu_seconds)
+        e["parity"] = greedy_parity(runner, rows, ref)
+    else:
+        cv, sample, cells, ref = oracle_cpu_rate(w, cpu_seconds)
+        e["parity"] = sample_parity(runner, 0, cells, ref)
+    e["cpu_baseline"] = baseline_entry(cv, unit, sample)
+    return e, runner
 
 
 # ------------------------------------------------------------------------------------- arms
@@ -502,19 +583,19 @@ def run_ours(args):
         line["ms_per_call"] = per_call_ms(runner, 64, args.warmup + args.steps)
         # end to end through the public API, from pinned host memory
         if not is_greedy:
-            ev, hb, db = e2e_rate(w, dev, max(3, min(args.steps, 10)))
+            ev, hb, db, ems = e2e_rate(w, dev, max(4, min(args.steps, 12)))
             line["e2e"] = {"value": round(ev * world, 1), "unit": unit, "h2d_bytes_per_step": hb,
-                           "d2h_bytes_per_step": db}
-        # the oracle on this host, bounded sample (N = 1 only)
-        if world > 1:
-            pass
-        elif is_greedy:
-            cv, sample, _ = oracle_cpu_rate_greedy(w, args.cpu_seconds)
-        else:
-            cv, sample, _ = oracle_cpu_rate(w, args.cpu_seconds)
+                           "d2h_bytes_per_step": db, "ms_per_step": round(ems, 4),
+                           "pipeline": "2 deep: next step's host->device copy overlaps this step's sampling"}
+        # the oracle on this host, bounded sample, and parity on that sample (N = 1 only)
         if world == 1:
-            line["cpu_baseline"] = {"value": round(cv, 2), "unit": unit, "cores": 1, "kind": "oracle",
-                                    "sample": sample, "host_cpus": os.cpu_count()}
+            if is_greedy:
+                cv, sample, rows, ref = oracle_cpu_rate_greedy(w, args.cpu_seconds)
+                line["parity"] = greedy_parity(runner, rows, ref)
+            else:
+                cv, sample, cells, ref = oracle_cpu_rate(w, args.cpu_seconds)
+                line["parity"] = sample_parity(runner, 0, cells, ref)
+            line["cpu_baseline"] = baseline_entry(cv, unit, sample)
         if not args.no_extra and wname == "cfg3" and world == 1:
             extra = {}
             nsteps = max(10, min(args.steps, 500))
@@ -527,28 +608,24 @@ def run_ours(args):
                 "f1_reveal": next_row_entry(
                     RevealRunner(runner, dev), nsteps, args.warmup,
                     "ds_reveal on one cfg3 step: 64 requests, C = 8, each commits 10% of its cells",
-                    "one CTA per request, 8 radix passes over L2-resident scores: latency-bound"),
+                    "L2-resident scores: latency-bound"),
             }
-            for other in ("cfg5", "cfg4"):
-                del runner
-                torch.cuda.empty_cache()
-                ow = make_workload(other)
-                runner = GreedyRunner(ow, dev) if other == "cfg4" else SampleRunner(ow, dev)
-                oms = time_steps(runner, max(10, min(args.steps, 1500)), args.warmup, 1)
-                extra[other] = {"workload": ow.name, "ms_per_step": round(oms, 5),
-                                "ms_per_call": per_call_ms(runner, 64, args.warmup + max(10, min(args.steps, 1500))),
-                                "units_per_s": round(runner.units / (oms / 1e3), 1),
-                                "roofline": roofline(runner.bytes_per_step, oms, other, dominant_kernel(ow))}
+            del runner
+            torch.cuda.empty_cache()
+            for other in ("cfg1", "cfg2", "cfg5", "cfg4"):
+                osteps = max(10, min(args.steps, 1500))
+                extra[other], orunner = config_entry(other, dev, osteps, args.warmup, args.cpu_seconds_other)
                 if other == "cfg4":
                     for dt, nm in ((torch.float32, "f4_log_softmax_f32"), (torch.bfloat16, "f4_log_softmax_bf16")):
                         nxt[nm] = next_row_entry(
-                            LogSoftmaxRunner(runner, dt), nsteps, args.warmup,
+                            LogSoftmaxRunner(orunner, dt), nsteps, args.warmup,
                             "ds_log_softmax on the cfg4 rows (256 x 248320), %s out" % str(dt).split(".")[-1],
                             "one read of the logits and one dense write; 4 rotating inputs")
                     nxt["f3_merge_triples"] = next_row_entry(
-                        MergeRunner(runner.pkg, dev), nsteps, args.warmup,
+                        MergeRunner(orunner.pkg, dev), nsteps, args.warmup,
                         "ds_merge_triples: 16384 tokens x 8 shards", "1.6 MB, L2-resident: launch-bound")
-                del ow
+                del orunner
+                torch.cuda.empty_cache()
             extra["next_rows"] = nxt
             line["also"] = extra
         print(json.dumps(line), flush=True)
@@ -571,9 +648,9 @@ def run_reference(args):
     sample = ""
     for i in range(args.warmup + args.steps):
         if is_greedy:
-            r, sample, _ = oracle_cpu_rate_greedy(w, budget)
+            r, sample, _, _ = oracle_cpu_rate_greedy(w, budget)
         else:
-            r, sample, _ = oracle_cpu_rate(w, budget, iteration=i % 32)
+            r, sample, _, _ = oracle_cpu_rate(w, budget, iteration=i % 32)
         if i >= args.warmup:
             rates.append(r)
     value = statistics.median(rates)
@@ -582,11 +659,47 @@ def run_reference(args):
             "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded, bf16 inputs)",
             "config": run_config(w, is_greedy, world),
-            "cpu_baseline": {"value": round(value, 2), "unit": unit, "cores": 1, "kind": "oracle",
-                             "sample": sample + " per step", "host_cpus": os.cpu_count()},
+            "cpu_baseline": baseline_entry(value, unit, sample + " per step"),
             "e2e": {"value": round(value, 2), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
+
+
+class _SleepStep:
+    """Launcher self-test step: 2 ms x (rank + 1) of wall time (no GPU work)."""
+
+    def __init__(self, rank):
+        self.rank = rank
+
+    def step(self, i):
+        time.sleep(0.002 * (self.rank + 1))
+
+    units = 1
+
+
+def run_selftest(args):
+    """The launch, timing and reporting path on CPU ranks (gloo), with a sleep for a step."""
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("gloo")
+    r = _SleepStep(rank)
+    ms = time_steps(r, args.steps, args.warmup, world, timer=HostTimer(), device="cpu")
+    if rank == 0:
+        print(json.dumps({"selftest": True, "metric": "launcher self-test (sleep steps, no GPU work)",
+                          "value": round(world * r.units / (ms / 1e3), 3), "unit": "steps/s", "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4)}), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def spawn_command(args, argv):
+    """Re-run this script under torch.distributed.run with one rank per GPU on this node."""
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(args.gpus),
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + argv
 
 
 def main():
@@ -596,13 +709,19 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["cfg3", "cfg5", "cfg4", "cfg1", "cfg2"], default="cfg3")
-    ap.add_argument("--no-extra", action="store_true", help="skip the large-vocab lines under 'also'")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-extra", action="store_true", help="skip the other configurations under 'also'")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle budget for the headline workload")
+    ap.add_argument("--cpu-seconds-other", type=float, default=4.0, help="oracle budget per other configuration")
     ap.add_argument("--ref-seconds-per-step", type=float, default=3.0)
+    ap.add_argument("--launch-selftest", action="store_true", help="multi-rank plumbing on CPU (gloo), no GPU work")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(subprocess.call(spawn_command(args, sys.argv[1:])))
+    if args.launch_selftest:
+        run_selftest(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

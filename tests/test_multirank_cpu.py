@@ -98,3 +98,22 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     with redirect_stdout(buf):
         assert bench.run_reference(args) is None
     assert buf.getvalue() == ""
+
+
+def test_gpus_flag_starts_one_rank_per_gpu():
+    """`bench.py --gpus 2` outside torchrun starts two ranks itself (torch.distributed.run on
+    127.0.0.1); the launcher self-test runs the same launch, timing and reporting path on CPU
+    ranks, so the line must say n_gpus 2 and carry the slower rank's time."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_PORT")}
+    env["OMP_NUM_THREADS"] = "1"
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--launch-selftest",
+                        "--steps", "5", "--warmup", "3"], capture_output=True, text=True, timeout=600, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["selftest"] is True and line["n_gpus"] == 2
+    # rank 1 sleeps 4 ms a step: the reported time is the max over ranks
+    assert line["ms_per_step"] >= 4.0

@@ -312,11 +312,13 @@ def test_misaligned_rows_and_u_alignment_differing_from_c():
         compare(inp, tok, lp, oracle_cells(inp, 8, 2), label="misaligned V=%d c+%d u+%d" % (V, c_off, u_off))
 
 
-@pytest.mark.parametrize("V", [2048, 2055, 2056])
+@pytest.mark.parametrize("V", [264, 520, 776, 2048, 2055, 2056])
 def test_warp_to_stream_switch_with_misaligned_rows(V):
     """Both sides of the switch from the one-warp-per-cell kernel (V <= 2055, where a lane holds
-    the most chunks and the longest scalar head or tail) to the streaming kernel (V >= 2056), with
-    c and u rows starting at odd 2-byte offsets that differ between c and u."""
+    the most chunks and the longest scalar head or tail) to the streaming kernel (V >= 2056), and
+    the smallest V of each chunk count of the warp kernel (256 (n - 1) + 8, where a row with a
+    7-element head fills exactly 32 (n - 1) chunks), with c and u rows starting at odd 2-byte
+    offsets that differ between c and u."""
     dev = _dev()
     inp = wl.make_sample_inputs("sw%d" % V, C=2, seq_lens=[3, 5, 2], V=V, guidance=[2.0, 0.0, 1.5],
                                 temperature=[0.9, 1.4, 0.0], sigma_c=3.0, sigma_u=1.5, top_ratio=0.1, seed=V)

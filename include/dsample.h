@@ -46,7 +46,7 @@ typedef enum {
 /* Limits of this build. */
 #define DS_MAX_ROWS 256          /* C: rows (codebooks) per call; the row index keys the noise */
 #define DS_MAX_ITERATION 16777215u /* iteration < 2^24; it keys the noise next to the row */
-#define DS_MAX_VOCAB 262137      /* largest V of ds_sample (16-CTA cluster, 16K elements per CTA) */
+#define DS_MAX_VOCAB 524281      /* largest V of ds_sample (16-CTA cluster, 32K elements per CTA) */
 
 /*
  * ds_sample -- sample every cell of a packed batch of guided logits.

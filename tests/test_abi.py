@@ -45,7 +45,7 @@ def test_status_strings(lib):
 
 
 def test_top_k_matches_oracle_definition(lib):
-    for V in (1, 2, 7, 100, 1025, 4097, 248320, 262137):
+    for V in (1, 2, 7, 100, 1025, 4097, 248320, 262137, 262144, 524281):
         for ratio in (1e-7, 0.001, 0.05, 0.1, 0.25, 1 / 3, 0.5, 0.9, 0.999, 1.0):
             assert pkg.top_k(ratio, V) == oracle.top_k(ratio, V), (ratio, V)
     assert pkg.top_k(0.0, 10) == 0 and pkg.top_k(1.5, 10) == 0 and pkg.top_k(0.5, 0) == 0

@@ -505,12 +505,13 @@ def test_keep_ties_mode(V, ratio):
 
 
 # ------------------------------------------------------------------------------------------ limits
+@pytest.mark.parametrize("V", [262144, pkg.DS_MAX_VOCAB])
 @pytest.mark.parametrize("ratio", [0.01, 0.5])
-def test_largest_vocabulary(ratio):
-    """V = DS_MAX_VOCAB on both large-vocabulary paths: the streaming pass with its fix-up (small
-    k) and the staged kernel alone with 16-CTA clusters (large k)."""
+def test_largest_vocabulary(ratio, V):
+    """V = 2^18 (a common vocabulary size) and V = DS_MAX_VOCAB on both large-vocabulary paths:
+    the streaming pass with its fix-up (small k) and the staged kernel alone with 16-CTA clusters
+    (large k; at DS_MAX_VOCAB each CTA holds 32768 elements, one CTA per SM)."""
     dev = _dev()
-    V = pkg.DS_MAX_VOCAB
     inp = wl.make_sample_inputs("vmax", C=1, seq_lens=[2, 3], V=V, guidance=[1.5, 0.0], temperature=[0.7, 1.2],
                                 sigma_c=4.0, sigma_u=2.0, top_ratio=ratio, seed=21)
     d = Dev(inp, dev)

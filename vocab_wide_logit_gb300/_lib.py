@@ -18,7 +18,7 @@ DS_ERR_CUDA = 3
 DS_DEV_ERR_LAYOUT = 1
 DS_DEV_ERR_NO_UNCOND = 2
 DS_DEV_ERR_PARAM = 4
-DS_MAX_VOCAB = 262137
+DS_MAX_VOCAB = 524281
 
 EXPORTED = ("ds_sample", "ds_greedy_lse", "ds_status_string", "ds_top_k", "ds_merge_triples", "ds_log_softmax",
             "ds_reveal", "ds_sample_ex", "ds_launch_count")

@@ -674,7 +674,10 @@ __global__ void __launch_bounds__(NT, 2) k_sample_cluster(const SampleArgs a, in
 namespace {
 constexpr int kClusterNT = 256;
 constexpr int kClusterUnroll = 8;
-constexpr int kSliceCapMax = 16384;
+// Elements per CTA: up to 32768 (16-bit slice-local indices; 192 KB of shared
+// memory, one CTA per SM at the largest slices), so 16-CTA clusters hold rows
+// of up to 16 x 32768 - 7 logits at any alignment.
+constexpr int kSliceCapMax = 32768;
 }  // namespace
 
 int cluster_kernel_max_vocab() { return 16 * kSliceCapMax - 7; }

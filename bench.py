@@ -349,14 +349,45 @@ class MergeRunner:
 
 
 def next_row_entry(runner, steps, warmup, workload, note):
-    """Device time and HBM roofline of one next-row entry point (same timing rules as the main line)."""
+    """Device time and HBM roofline of one next-row entry point (same timing rules as the main line),
+    and the per-call device time from a CUDA-graph replay (latency-bound calls are otherwise timed at
+    the host's issue rate)."""
     ms = time_steps(runner, steps, warmup, 1)
     peak, src = hbm_peak()
     gbs = runner.bytes_per_step / (ms / 1e3) / 1e9
-    return {"workload": workload, "ms_per_call": round(ms, 5),
+    return {"workload": workload, "ms_per_call": round(ms, 5), "ms_per_call_graph": graph_call_ms(runner),
             "units_per_s": round(runner.units / (ms / 1e3), 1),
             "algorithmic_bytes_per_call": runner.bytes_per_step, "achieved_gbs": round(gbs, 1),
             "frac": round(gbs / peak, 4), "peak": peak, "peak_source": src, "note": note}
+
+
+def graph_call_ms(runner, calls=20, reps=5):
+    """Device time per call with the host out of the way: `calls` calls captured in one CUDA graph
+    and replayed (each call's launches and their programmatic dependencies become graph nodes), so
+    a latency-bound call is not timed at the rate the host can issue it. Median over replays."""
+    st = torch.cuda.Stream()
+    runner.step(0)  # launch settings are looked up and kept before capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g, stream=st):
+            for i in range(calls):
+                runner.step(i)
+    except RuntimeError as e:  # reported, not fatal: the stream-issued numbers stand
+        torch.cuda.synchronize()
+        return "graph capture failed: %s" % str(e).splitlines()[0][:200]
+    t = []
+    with torch.cuda.stream(st):  # replay and its events on one stream
+        g.replay()
+        torch.cuda.synchronize()
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            g.replay()
+            b.record(st)
+            torch.cuda.synchronize()
+            t.append(a.elapsed_time(b) / calls)
+    return round(statistics.median(t), 5)
 
 
 def per_call_ms(runner, calls, first_step):
@@ -533,6 +564,7 @@ def config_entry(name, dev, steps, warmup, cpu_seconds):
     unit = "rows/s" if is_greedy else "sampled positions/s"
     e = {"workload": w.name, "ms_per_step": round(ms, 5), "us_per_step": round(ms * 1e3, 2),
          "ms_per_call": per_call_ms(runner, 64, warmup + steps),
+         "us_per_call_graph": round(1e3 * graph_call_ms(runner), 2),
          "units_per_s": round(runner.units / (ms / 1e3), 1), "unit": unit,
          "roofline": roofline(runner.bytes_per_step, ms, name, dominant_kernel(w))}
     if is_greedy:

@@ -538,3 +538,17 @@ def test_most_rows_last_iteration_and_many_requests():
     cells = np.sort(rng.choice(inp.C * inp.P, size=4000, replace=False))
     compare(inp, tok, lp, oracle_cells(inp, 2 ** 63 + 5, it, cells), cells, label="limits")
     assert int(d.status.item()) == 0
+
+
+def test_alternating_shapes_reuse_launch_settings():
+    """The library keeps each kernel's launch settings per device (shared-memory limit, occupancy).
+    Calls whose staged slices shrink and grow again (V = 248320, then 9000, then 248320 on the staged
+    kernel, and the streaming pass in between) must each launch and match the oracle."""
+    dev = _dev()
+    for V, ratio in ((248320, 0.5), (9000, 0.5), (248320, 0.05), (9000, 0.6), (248320, 0.5)):
+        inp = wl.make_sample_inputs("alt%d" % V, C=1, seq_lens=[2, 1], V=V, guidance=[1.5, 0.0],
+                                    temperature=[0.7, 1.1], sigma_c=3.0, sigma_u=1.0, top_ratio=ratio, seed=V % 97)
+        d = Dev(inp, dev)
+        tok, lp = d.run(5, 1)
+        compare(inp, tok, lp, oracle_cells(inp, 5, 1), label="alt V=%d ratio %g" % (V, ratio))
+        assert int(d.status.item()) == 0

@@ -7,6 +7,9 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <cuda_runtime.h>
 
 #include "dsample.h"
@@ -31,28 +34,42 @@ double normal_upper_quantile(double p) {
   return 0.5 * (lo + hi);
 }
 
-// SM count of the current device, cached per device (callers on several host
-// threads may race to fill an entry; they store the same value).
-int device_sm_count() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  static std::atomic<int> cache[64];
-  if (dev >= 0 && dev < 64) {
-    const int v = cache[dev].load(std::memory_order_relaxed);
-    if (v > 0) return v;
-  }
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  if (dev >= 0 && dev < 64) cache[dev].store(sms, std::memory_order_relaxed);
-  return sms;
+std::atomic<unsigned long long> g_launches{0};
+
+std::mutex g_cache_mu;
+std::map<std::tuple<const void*, int, long long>, int>& launch_cache() {
+  static std::map<std::tuple<const void*, int, long long>, int> m;
+  return m;
 }
 
-std::atomic<unsigned long long> g_launches{0};
+int device_sm_count() { return ds::device_sms(); }
 
 }  // namespace
 
 namespace ds {
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+bool cache_lookup(const void* site, int dev, long long param, int* value) {
+  std::lock_guard<std::mutex> lk(g_cache_mu);
+  const auto& m = launch_cache();
+  const auto it = m.find(std::make_tuple(site, dev, param));
+  if (it == m.end()) return false;
+  *value = it->second;
+  return true;
+}
+
+void cache_store(const void* site, int dev, long long param, int value) {
+  std::lock_guard<std::mutex> lk(g_cache_mu);
+  launch_cache()[std::make_tuple(site, dev, param)] = value;
+}
+
+int device_sms() {
+  static const char site = 0;
+  return cached(&site, 0, [](int dev) {
+    int sms = 0;
+    return cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? sms : -1;
+  });
+}
 }  // namespace ds
 
 extern "C" {

@@ -11,6 +11,27 @@ namespace ds {
 // Counts every kernel the library launches (read by ds_launch_count).
 void note_launch();
 
+// Launch-time queries (a kernel's occupancy, its shared-memory attribute, the
+// SM count) cost microseconds of host time each; their answers depend only on
+// the device, the kernel and its shared memory. cached(site, param, init) runs
+// init(device) the first time a (site, current device, param) key is seen and
+// returns its positive result from then on (a result <= 0 is an error and is
+// not kept). Thread-safe.
+bool cache_lookup(const void* site, int dev, long long param, int* value);
+void cache_store(const void* site, int dev, long long param, int value);
+template <typename F>
+int cached(const void* site, long long param, F init) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  int v = 0;
+  if (cache_lookup(site, dev, param, &v)) return v;
+  v = init(dev);
+  if (v > 0) cache_store(site, dev, param, v);
+  return v;
+}
+// SM count of the current device (cached).
+int device_sms();
+
 constexpr int kWarpKernelThreads = 128;
 constexpr int kStreamMark = DS_MARKED_TOKEN;  // out_tokens marker left by a fast pass for the exact one
 

@@ -221,13 +221,15 @@ cudaError_t launch_greedy(const uint16_t* x, int n, int V, float* out_max, float
   constexpr int NT = 512;
   constexpr int UNROLL = 4;
   auto kern = k_greedy_lse<NT, UNROLL>;
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, 0);
-  if (e != cudaSuccess) return e;
+  const int sms = device_sms();
+  if (sms <= 0) return cudaErrorUnknown;
+  const int per_sm = cached(reinterpret_cast<const void*>(kern), 0, [&](int) {
+    int v = 0;
+    const cudaError_t r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, NT, 0);
+    return r != cudaSuccess ? -(int)r : (v < 1 ? 1 : v);
+  });
+  if (per_sm <= 0) return per_sm < 0 ? (cudaError_t)(-per_sm) : cudaErrorUnknown;
+  cudaError_t e;
   // Split each row over a cluster of cs CTAs so that all rows' CTAs fit in one
   // wave when they can (no tail wave), with at least one 16-byte chunk per
   // thread and at most 8 CTAs per row.

@@ -297,8 +297,6 @@ cudaError_t launch_log_softmax_fused(const uint16_t* x, int n, int V, float* out
   if (cs > 8) return cudaErrorInvalidValue;
   const size_t smem = (size_t)((nq + cs - 1) / cs) * sizeof(uint4);
   auto kern = bf16_out ? k_log_softmax_fused<true> : k_log_softmax_fused<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kLsNT, 1, 1);
   cfg.dynamicSmemBytes = smem;
@@ -316,13 +314,29 @@ cudaError_t launch_log_softmax_fused(const uint16_t* x, int n, int V, float* out
   // No cluster of this shape fits the device (the query fails or finds none):
   // refuse before launching anything, so the caller can take the two-pass form.
   // Only the query's own error is cleared here.
-  int max_clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-  if (e != cudaSuccess) (void)cudaGetLastError();
-  if (e != cudaSuccess || max_clusters < 1) {
+  // (the shared-memory limit, one value per kernel, is set once per device for
+  // the largest slice; the occupancy is kept per device and shape; a refusal is
+  // asked again next time)
+  const int attr_ok = cached(reinterpret_cast<const void*>(kern), -1, [&](int) {
+    const cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)((size_t)kLsSliceMax * sizeof(uint4)));
+    if (r != cudaSuccess) (void)cudaGetLastError();
+    return r == cudaSuccess ? 1 : 0;
+  });
+  const int max_clusters = attr_ok <= 0 ? 0 : cached(reinterpret_cast<const void*>(kern), (long long)smem * 16 + cs, [&](int) {
+    int v = 0;
+    const cudaError_t r = cudaOccupancyMaxActiveClusters(&v, kern, &cfg);
+    if (r != cudaSuccess) {
+      (void)cudaGetLastError();
+      return 0;
+    }
+    return v;
+  });
+  if (max_clusters < 1) {
     *refused = true;
     return cudaSuccess;
   }
+  cudaError_t e;
   long long n_clusters = max_clusters;
   if (n_clusters > n) n_clusters = n;
   cfg.gridDim = dim3((unsigned)(n_clusters * cs), 1, 1);

@@ -121,11 +121,9 @@ __global__ void __launch_bounds__(256) k_log_softmax_write(const uint16_t* __res
 }
 
 static cudaError_t launch_plain(const void* kern, void** args, long long work, cudaStream_t st) {
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
+  const int sms = device_sms();
+  if (sms <= 0) return cudaErrorUnknown;
+  cudaError_t e;
   long long blocks = (work + 255) / 256;
   const long long cap = (long long)sms * 8;
   if (blocks > cap) blocks = cap;
@@ -154,11 +152,9 @@ cudaError_t launch_merge_triples(const float* triples, int n, int shards, float*
 cudaError_t launch_log_softmax_write(const uint16_t* x, int n, int V, const float* lse, void* out, bool bf16_out,
                                      cudaStream_t st) {
   if (n <= 0 || V <= 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
+  const int sms = device_sms();
+  if (sms <= 0) return cudaErrorUnknown;
+  cudaError_t e;
   // rows on y; per row enough blocks on x that the grid holds about 8 blocks per
   // SM, but no more than the row's chunks need at 4 per thread
   const int by = n < 65535 ? n : 65535;

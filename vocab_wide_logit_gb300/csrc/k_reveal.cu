@@ -6,10 +6,12 @@
 // top reveal_count. One CTA per request finds the reveal_count-th cell of the
 // order (score desc, flattened index asc) and scatters the tokens of the cells
 // up to it into the canvas. A request of at most kRevealStaged cells is staged
-// once in shared memory as 32-bit score keys: four 8-bit radix rounds find the
-// k-th key H, and the cells tied at H are taken in index order by a prefix
-// count. A larger request runs an exact 64-bit radix select (score key above
-// the inverted flattened index, so keys are distinct) over global memory.
+// once in shared memory as 32-bit score keys: a 2-bit radix select (16 rounds
+// of counting by warp reductions, one barrier each, no atomics) finds the k-th
+// key H, and when cells tied at H straddle the cut, a binary search over the
+// flattened index finds the last one revealed. A larger request runs an exact
+// 64-bit radix select (score key above the inverted flattened index, so keys
+// are distinct) over global memory.
 #include <climits>
 
 #include "ds_device.cuh"
@@ -19,7 +21,9 @@ namespace ds {
 
 namespace {
 
-constexpr int kRevealNT = 1024;  // short passes: a request holds about 2000 cells
+// A request holds about 2000 cells: 1024 threads give 2 keys per thread per
+// round (16.7 us per config-3 call, against 18.0 and 19.7 us at 512 and 256).
+constexpr int kRevealNT = 1024;
 constexpr int kRevealStaged = 16384;  // cells staged in shared memory (64 KB of keys)
 
 // Larger key = earlier in the reveal order: the score's order-preserving bits
@@ -60,6 +64,25 @@ __device__ __forceinline__ void pick_digit(const int* hist, int need, int lane, 
 
 }  // namespace
 
+// Block-wide sums of three per-thread counts (one barrier: each warp writes
+// its sums to its slot of this round's buffer, every thread adds them up).
+__device__ __forceinline__ int3 block_sum3(int a, int b, int c, int (*slots)[kRevealNT / 32][4], int parity) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  a = __reduce_add_sync(0xffffffffu, a);
+  b = __reduce_add_sync(0xffffffffu, b);
+  c = __reduce_add_sync(0xffffffffu, c);
+  if (lane == 0) {
+    slots[parity][wid][0] = a;
+    slots[parity][wid][1] = b;
+    slots[parity][wid][2] = c;
+  }
+  __syncthreads();
+  // lane w reads warp w's sums; three warp reductions give every lane the totals
+  const int4 v = (lane < kRevealNT / 32) ? *reinterpret_cast<const int4*>(slots[parity][lane]) : make_int4(0, 0, 0, 0);
+  return make_int3(__reduce_add_sync(0xffffffffu, v.x), __reduce_add_sync(0xffffffffu, v.y),
+                   __reduce_add_sync(0xffffffffu, v.z));
+}
+
 __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ scores,
                                                       const int32_t* __restrict__ tokens,
                                                       const int32_t* __restrict__ seq_lens,
@@ -67,18 +90,17 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
                                                       int32_t* __restrict__ canvas, uint8_t* __restrict__ revealed,
                                                       uint32_t* __restrict__ d_status) {
   __shared__ int hist[256];
-  __shared__ long long s_tot, s_off;
-  __shared__ int s_bad;
+  __shared__ __align__(16) int slots[2][kRevealNT / 32][4];
   __shared__ unsigned long long s_prefix;
   __shared__ int s_need;
-  __shared__ int s_wcnt[kRevealNT / 32];
   extern __shared__ uint32_t skeys[];  // the staged request's score keys, in flattened order
   pdl_release();
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int parity = 0;
 
   for (int r = blockIdx.x; r < B; r += gridDim.x) {
-    // the request's offset and the batch total, by a block-wide sum
+    // the request's offset and the batch total (sums of non-negative int32, in 64 bits)
     long long off = 0, tot = 0;
     int bad = 0;
     for (int j = tid; j < B; j += kRevealNT) {
@@ -88,21 +110,33 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
       tot += Tc;
       if (j < r) off += Tc;
     }
-    if (tid == 0) {
-      s_tot = 0;
-      s_off = 0;
-      s_bad = 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      off += __shfl_xor_sync(0xffffffffu, off, o);
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    __syncthreads();  // the previous request is done with the slots
+    if (lane == 0) {
+      reinterpret_cast<long long*>(slots[0])[wid] = off;
+      reinterpret_cast<long long*>(slots[1])[wid] = tot;
+      hist[wid] = bad;
     }
     __syncthreads();
-    atomicAdd(reinterpret_cast<unsigned long long*>(&s_tot), (unsigned long long)tot);
-    atomicAdd(reinterpret_cast<unsigned long long*>(&s_off), (unsigned long long)off);
-    if (bad) atomicOr(&s_bad, 1);
-    __syncthreads();
-    if (s_bad || s_tot != (long long)P) {
+    off = 0;
+    tot = 0;
+    bad = 0;
+#pragma unroll
+    for (int w = 0; w < kRevealNT / 32; ++w) {
+      off += reinterpret_cast<const long long*>(slots[0])[w];
+      tot += reinterpret_cast<const long long*>(slots[1])[w];
+      bad |= hist[w];
+    }
+    if (bad || tot != (long long)P) {
       if (tid == 0 && r == (int)blockIdx.x) report(d_status, DS_DEV_ERR_LAYOUT);
       return;  // uniform across the CTA; the layout is invalid for every request
     }
-    const long long roff = s_off;
+    const long long roff = off;
     const int T = seq_lens[r];
     const long long n = (long long)C * T;
     long long k = reveal_counts[r];
@@ -113,61 +147,84 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
     };
 
     if (k > 0 && k < n && n <= kRevealStaged) {
+      // n < 2^15 here: 32-bit index arithmetic
       const int nn = (int)n, kk = (int)k;
-      for (int f = tid; f < nn; f += kRevealNT) skeys[f] = score_key(scores[cell_of(f)]);
-      if (tid == 0) {
-        s_prefix = 0ull;
-        s_need = kk;
-      }
+      const unsigned Tu = (unsigned)T;
+      auto cell32 = [&](int f) -> long long {
+        const unsigned c = (unsigned)f / Tu;
+        return (long long)c * P + roff + (long long)((unsigned)f - c * Tu);
+      };
+      for (int f = tid; f < nn; f += kRevealNT) skeys[f] = score_key(scores[cell32(f)]);
       __syncthreads();
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int b = tid; b < 256; b += kRevealNT) hist[b] = 0;
-        __syncthreads();
-        const uint32_t prefix = (uint32_t)s_prefix;
+      // 2-bit radix select of the kk-th largest key H, MSB first: each round
+      // counts, among the keys that match H above the current digit, those
+      // whose digit is >= 1, 2 and 3; one barrier per round, no atomics
+      uint32_t H = 0u;
+      int need = kk;  // H's rank among the keys matching the prefix
+      int eq_cnt = nn;
+#pragma unroll 1
+      for (int shift = 30; shift >= 0; shift -= 2) {
+        int c1 = 0, c2 = 0, c3 = 0;
+        const uint32_t hi_mask = (shift == 30) ? 0u : (0xffffffffu << (shift + 2));
         for (int f = tid; f < nn; f += kRevealNT) {
           const uint32_t key = skeys[f];
-          if (shift == 24 || (key >> (shift + 8)) == (prefix >> (shift + 8))) atomicAdd(&hist[(key >> shift) & 255u], 1);
-        }
-        __syncthreads();
-        if (wid == 0) {
-          int digit, above;
-          pick_digit(hist, s_need, lane, digit, above);
-          if (digit >= 0) {
-            s_prefix = (unsigned long long)(prefix | ((uint32_t)digit << shift));
-            s_need -= above;
+          if ((key & hi_mask) == (H & hi_mask)) {
+            const uint32_t d = (key >> shift) & 3u;
+            c1 += d >= 1u;
+            c2 += d >= 2u;
+            c3 += d >= 3u;
           }
         }
-        __syncthreads();
-      }
-      // every key above H is revealed; of the keys equal to H, the first `need`
-      // in flattened order (a running count over chunks of kRevealNT cells)
-      const uint32_t H = (uint32_t)s_prefix;
-      const int need = s_need;
-      int run = 0;
-      for (int base = 0; base < nn; base += kRevealNT) {
-        const int f = base + tid;
-        const uint32_t key = (f < nn) ? skeys[f] : 0u;
-        const bool tied = f < nn && key == H;
-        const unsigned bt = __ballot_sync(0xffffffffu, tied);
-        if (lane == 0) s_wcnt[wid] = __popc(bt);
-        __syncthreads();
-        int before = run, total = 0;
-#pragma unroll
-        for (int w = 0; w < kRevealNT / 32; ++w) {
-          const int cw = s_wcnt[w];
-          before += (w < wid) ? cw : 0;
-          total += cw;
+        const int3 cs = block_sum3(c1, c2, c3, slots, parity);
+        parity ^= 1;
+        const int cnt_prefix = eq_cnt;  // keys matching the prefix before this digit
+        uint32_t d;
+        if (cs.z >= need) {
+          d = 3u;
+          eq_cnt = cs.z;
+        } else if (cs.y >= need) {
+          d = 2u;
+          need -= cs.z;
+          eq_cnt = cs.y - cs.z;
+        } else if (cs.x >= need) {
+          d = 1u;
+          need -= cs.y;
+          eq_cnt = cs.x - cs.y;
+        } else {
+          d = 0u;
+          need -= cs.x;
+          eq_cnt = cnt_prefix - cs.x;
         }
-        before += __popc(bt & ((1u << lane) - 1u));
-        if (f < nn) {
-          const bool on = key > H || (tied && before < need);
-          const long long cell = cell_of(f);
-          if (on) canvas[cell] = tokens[cell];
-          if (revealed) revealed[cell] = on ? 1 : 0;
-        }
-        run += total;
-        __syncthreads();  // s_wcnt is rewritten by the next chunk
+        H |= d << shift;
       }
+      // every key above H is revealed; of the eq_cnt keys equal to H, the first
+      // `need` in flattened order: the need-th one's index by a binary search
+      // (only when ties straddle the cut)
+      int f_cut = nn;  // keys equal to H with f < f_cut are revealed
+      if (eq_cnt > need) {
+        int lo = 0, hi = nn - 1;
+#pragma unroll 1
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          int c = 0;
+          for (int f = tid; f <= mid; f += kRevealNT) c += skeys[f] == H;
+          const int3 cs = block_sum3(c, 0, 0, slots, parity);
+          parity ^= 1;
+          if (cs.x >= need)
+            hi = mid;
+          else
+            lo = mid + 1;
+        }
+        f_cut = lo + 1;
+      }
+      for (int f = tid; f < nn; f += kRevealNT) {
+        const uint32_t key = skeys[f];
+        const bool on = key > H || (key == H && f < f_cut);
+        const long long cell = cell32(f);
+        if (on) canvas[cell] = tokens[cell];
+        if (revealed) revealed[cell] = on ? 1 : 0;
+      }
+      __syncthreads();  // skeys is restaged by the next request
       continue;  // uniform across the CTA
     }
 
@@ -213,16 +270,17 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
 cudaError_t launch_reveal(const float* scores, const int32_t* tokens, const int32_t* seq_lens,
                           const int32_t* reveal_counts, int B, int C, int P, int32_t* canvas, uint8_t* revealed,
                           uint32_t* d_status, cudaStream_t st) {
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_reveal, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)(kRevealStaged * sizeof(uint32_t)));
-  if (e != cudaSuccess) return e;
+  const int sms = device_sms();
+  if (sms <= 0) return cudaErrorUnknown;
+  const int ok = cached(reinterpret_cast<const void*>(k_reveal), 0, [](int) {
+    const cudaError_t r = cudaFuncSetAttribute(k_reveal, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(kRevealStaged * sizeof(uint32_t)));
+    return r == cudaSuccess ? 1 : -(int)r;
+  });
+  if (ok <= 0) return ok < 0 ? (cudaError_t)(-ok) : cudaErrorUnknown;
+  cudaError_t e;
   long long blocks = B;
-  if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+  if (blocks > (long long)sms * 4) blocks = (long long)sms * 4;
   if (blocks < 1) blocks = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks, 1, 1);

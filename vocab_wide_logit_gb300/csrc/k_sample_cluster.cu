@@ -690,12 +690,6 @@ cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st, int only
   if (slice_cap > kSliceCapMax) return cudaErrorInvalidValue;
   auto kern = k_sample_cluster<kClusterNT, kClusterUnroll>;
   const size_t smem = (size_t)slice_cap * (sizeof(float) + sizeof(uint16_t));
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  if (cs > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kClusterNT, 1, 1);
   cfg.dynamicSmemBytes = smem;
@@ -710,10 +704,24 @@ cudaError_t launch_sample_cluster(const SampleArgs& a, cudaStream_t st, int only
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   cfg.gridDim = dim3((unsigned)cs, 1, 1);
-  int max_clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-  if (e != cudaSuccess) return e;
+  // the kernel's attributes, set once per device for its largest slice (the
+  // shared-memory limit is one value per kernel), then the cluster occupancy,
+  // kept per device and shape
+  const int attrs = cached(reinterpret_cast<const void*>(kern), -1, [&](int) {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)((size_t)kSliceCapMax * (sizeof(float) + sizeof(uint16_t))));
+    if (r == cudaSuccess) r = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return r == cudaSuccess ? 1 : -(int)r;
+  });
+  if (attrs <= 0) return attrs < 0 ? (cudaError_t)(-attrs) : cudaErrorUnknown;
+  const int max_clusters = cached(reinterpret_cast<const void*>(kern), (long long)smem * 32 + cs, [&](int) {
+    int v = 0;
+    const cudaError_t r = cudaOccupancyMaxActiveClusters(&v, kern, &cfg);
+    return r != cudaSuccess ? -(int)r : v;
+  });
+  if (max_clusters < 0) return (cudaError_t)(-max_clusters);
   if (max_clusters < 1) return cudaErrorLaunchOutOfResources;
+  cudaError_t e;
   const long long n_cells = (long long)a.C * a.P;
   long long n_clusters = max_clusters;
   // in fix-up mode the marked cells are rare: a few clusters scan the markers

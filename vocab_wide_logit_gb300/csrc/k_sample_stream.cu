@@ -757,10 +757,13 @@ cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
   auto kern = aligned ? k_sample_stream<kStreamNT, kStreamUnroll, true>
                       : k_sample_stream<kStreamNT, kStreamUnroll, false>;
   const size_t smem = sizeof(WarpArea) * (kStreamNT / 32);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  const int attr_ok = cached(reinterpret_cast<const void*>(kern), (long long)smem, [&](int) {
+    const cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return r == cudaSuccess ? 1 : -(int)r;
+  });
+  if (attr_ok <= 0) return attr_ok < 0 ? (cudaError_t)(-attr_ok) : cudaErrorUnknown;
   int dev = 0;
-  e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   long long cap[5] = {0, 0, 0, 0, 0};
   for (int cs = 1; cs <= cs_max; cs *= 2) {

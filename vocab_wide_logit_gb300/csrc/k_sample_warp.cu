@@ -413,12 +413,14 @@ template <int NCH, bool FULL>
 static cudaError_t launch_nch(const SampleArgs& a, cudaStream_t st, int num_sms, int only_marked) {
   const size_t smem = (size_t)(kWarpKernelThreads / 32) * sizeof(WarpSmem<NCH>);
   auto kern = k_sample_warp<NCH, FULL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarpKernelThreads, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
+  const int per_sm = cached(reinterpret_cast<const void*>(kern), (long long)smem, [&](int) {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int n = 0;
+    if (r == cudaSuccess) r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarpKernelThreads, smem);
+    return r != cudaSuccess ? -(int)r : (n < 1 ? 1 : n);
+  });
+  if (per_sm <= 0) return per_sm < 0 ? (cudaError_t)(-per_sm) : cudaErrorUnknown;
+  cudaError_t e;
   const long long n_cells = (long long)a.C * a.P;
   long long blocks = (long long)num_sms * per_sm;
   const long long max_useful = (n_cells + (kWarpKernelThreads / 32) - 1) / (kWarpKernelThreads / 32);

@@ -45,7 +45,7 @@ FALLBACK_HBM_GBS = 6800.0
 # The sources that define each workload's kernels and their launch plan: its
 # committed DRAM figure stays valid while their code is unchanged.
 KERNEL_SOURCES = {
-    "cfg3": ["ds_device.cuh", "ds_sample_common.cuh", "k_sample_warp.cu"],
+    "cfg3": ["ds_device.cuh", "ds_sample_common.cuh", "ds_warp_common.cuh", "k_sample_warp.cu"],
     "cfg5": ["ds_device.cuh", "ds_sample_common.cuh", "k_sample_stream.cu", "k_sample_cluster.cu"],
     "cfg4": ["ds_device.cuh", "k_greedy.cu"],
 }

@@ -168,9 +168,21 @@ constexpr float kExactGFrom = 6.0f;
 // ALIGNED: every c and u row starts on a 16-byte boundary (V a multiple of 8,
 // both buffers 16-byte aligned), so chunks never straddle rows and u never
 // needs the element-wise gather.
+// Programmatic-launch roles of a streaming launch (the call's kernels run in
+// stream order; see launch_sample_stream):
+//   kPdlAlone  wait for the previous kernel first, let the next one launch last
+//   kPdlHead   the first of two launches: wait first, then let the tail launch
+//              go at once (its CTAs take SM room only as this grid's CTAs exit)
+//   kPdlTail   the second: its cells are its own and it reads only inputs, so
+//              it starts without waiting; it waits for the head grid before it
+//              exits, so that the pass behind it sees both launches complete
+constexpr int kPdlAlone = 0, kPdlHead = 1, kPdlTail = 2;
+
 template <int NT, int UNROLL, bool ALIGNED>
-__global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, long long cell_lo, long long cell_hi) {
-  pdl_wait();
+__global__ void __launch_bounds__(NT, 3)
+    k_sample_stream(const SampleArgs a, long long cell_lo, long long cell_hi, int pdl_role) {
+  if (pdl_role != kPdlTail) pdl_wait();
+  if (pdl_role == kPdlHead) pdl_release();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ SXchg xs;
   __shared__ SRec wrec[NT / 32];
@@ -212,6 +224,8 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, lon
       }
       report(a.d_status, DS_DEV_ERR_LAYOUT);
     }
+    if (pdl_role == kPdlTail) pdl_wait();
+    if (pdl_role != kPdlHead) pdl_release();
     return;  // uniform across the cluster; no shared memory was shared yet
   }
   cl.sync();  // peers may write s_sa from here on
@@ -698,10 +712,12 @@ __global__ void __launch_bounds__(NT, 3) k_sample_stream(const SampleArgs a, lon
     }
     __syncthreads();
   }
-  // The next kernel (the fix-up pass) may start launching only now: this grid
-  // is persistent and sized for an empty GPU, so no dependent grid should take
-  // SM room before its cells are done.
-  pdl_release();
+  // The next kernel (the fix-up pass, or the tail launch already released by a
+  // head launch) may start launching only now: this grid is persistent and sized
+  // for an empty GPU, so the pass behind it should not take SM room before its
+  // cells are done. A tail launch first waits for the head grid.
+  if (pdl_role == kPdlTail) pdl_wait();
+  if (pdl_role != kPdlHead) pdl_release();
   cl.sync();  // no CTA leaves while a peer may still read its exchange slots or write s_sa
 }
 
@@ -797,7 +813,7 @@ cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
       }
     }
   }
-  auto launch = [&](int cs, long long lo, long long hi) -> cudaError_t {
+  auto launch = [&](int cs, long long lo, long long hi, int role) -> cudaError_t {
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kStreamNT, 1, 1);
     cfg.dynamicSmemBytes = smem;
@@ -814,13 +830,17 @@ cudaError_t launch_sample_stream(const SampleArgs& a, cudaStream_t st) {
     long long n_clusters = cap[cs];
     if (n_clusters > hi - lo) n_clusters = hi - lo;
     cfg.gridDim = dim3((unsigned)(n_clusters * cs), 1, 1);
-    cudaError_t r = cudaLaunchKernelEx(&cfg, kern, a, lo, hi);
+    cudaError_t r = cudaLaunchKernelEx(&cfg, kern, a, lo, hi, role);
     if (r != cudaSuccess) return r;
     note_launch();
     return cudaGetLastError();
   };
-  e = launch(cs1, 0, split);
-  if (e == cudaSuccess && split < n_cells) e = launch(cs2, split, n_cells);
+  if (split < n_cells) {
+    e = launch(cs1, 0, split, kPdlHead);
+    if (e == cudaSuccess) e = launch(cs2, split, n_cells, kPdlTail);
+  } else {
+    e = launch(cs1, 0, split, kPdlAlone);
+  }
   return e;
 }
 

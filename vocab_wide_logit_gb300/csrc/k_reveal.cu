@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
   __shared__ int hist[256];
   __shared__ __align__(16) int slots[2][kRevealNT / 32][4];
   __shared__ unsigned long long s_prefix;
-  __shared__ int s_need;
+  __shared__ int s_need, s_eq;
   extern __shared__ uint32_t skeys[];  // the staged request's score keys, in flattened order
   pdl_release();
   pdl_wait();
@@ -157,11 +157,10 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
       for (int f = tid; f < nn; f += kRevealNT) skeys[f] = score_key(scores[cell32(f)]);
       __syncthreads();
       // 2-bit radix select of the kk-th largest key H, MSB first: each round
-      // counts, among the keys that match H above the current digit, those
-      // whose digit is >= 1, 2 and 3; one barrier per round, no atomics
+      // every warp counts, among its keys that match H above the current digit,
+      // those whose digit is >= 1, 2 and 3; warp 0 adds the warps' counts, picks
+      // the digit and publishes the new prefix (two barriers a round, no atomics)
       uint32_t H = 0u;
-      int need = kk;  // H's rank among the keys matching the prefix
-      int eq_cnt = nn;
 #pragma unroll 1
       for (int shift = 30; shift >= 0; shift -= 2) {
         int c1 = 0, c2 = 0, c3 = 0;
@@ -175,28 +174,50 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
             c3 += d >= 3u;
           }
         }
-        const int3 cs = block_sum3(c1, c2, c3, slots, parity);
-        parity ^= 1;
-        const int cnt_prefix = eq_cnt;  // keys matching the prefix before this digit
-        uint32_t d;
-        if (cs.z >= need) {
-          d = 3u;
-          eq_cnt = cs.z;
-        } else if (cs.y >= need) {
-          d = 2u;
-          need -= cs.z;
-          eq_cnt = cs.y - cs.z;
-        } else if (cs.x >= need) {
-          d = 1u;
-          need -= cs.y;
-          eq_cnt = cs.x - cs.y;
-        } else {
-          d = 0u;
-          need -= cs.x;
-          eq_cnt = cnt_prefix - cs.x;
+        c1 = __reduce_add_sync(0xffffffffu, c1);
+        c2 = __reduce_add_sync(0xffffffffu, c2);
+        c3 = __reduce_add_sync(0xffffffffu, c3);
+        if (lane == 0) {
+          slots[0][wid][0] = c1;
+          slots[0][wid][1] = c2;
+          slots[0][wid][2] = c3;
         }
-        H |= d << shift;
+        __syncthreads();
+        if (wid == 0) {
+          const int4 v = (lane < kRevealNT / 32) ? *reinterpret_cast<const int4*>(slots[0][lane]) : make_int4(0, 0, 0, 0);
+          const int C1 = __reduce_add_sync(0xffffffffu, v.x), C2 = __reduce_add_sync(0xffffffffu, v.y),
+                    C3 = __reduce_add_sync(0xffffffffu, v.z);
+          int need = (shift == 30) ? kk : s_need;
+          int eq = (shift == 30) ? nn : s_eq;
+          uint32_t d;
+          if (C3 >= need) {
+            d = 3u;
+            eq = C3;
+          } else if (C2 >= need) {
+            d = 2u;
+            need -= C3;
+            eq = C2 - C3;
+          } else if (C1 >= need) {
+            d = 1u;
+            need -= C2;
+            eq = C1 - C2;
+          } else {
+            d = 0u;
+            need -= C1;
+            eq = eq - C1;
+          }
+          __syncwarp();
+          if (lane == 0) {
+            s_prefix = (unsigned long long)(H | (d << shift));
+            s_need = need;
+            s_eq = eq;
+          }
+        }
+        __syncthreads();
+        H = (uint32_t)s_prefix;
       }
+      const int need = s_need;
+      const int eq_cnt = s_eq;
       // every key above H is revealed; of the eq_cnt keys equal to H, the first
       // `need` in flattened order: the need-th one's index by a binary search
       // (only when ties straddle the cut)

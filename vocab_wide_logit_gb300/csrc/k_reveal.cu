@@ -24,6 +24,10 @@ namespace {
 // A request holds about 2000 cells: 1024 threads give 2 keys per thread per
 // round (16.7 us per config-3 call, against 18.0 and 19.7 us at 512 and 256).
 constexpr int kRevealNT = 1024;
+// Warps that run the select rounds: 16 (15.0 us per config-3 call on the
+// device, against 17.4, 22.0 and 33.1 us with 8, 4 and 2, and 16.4 us with all 32
+// behind block barriers).
+constexpr int kSelWarps = 16;
 constexpr int kRevealStaged = 16384;  // cells staged in shared memory (64 KB of keys)
 
 // Larger key = earlier in the reveal order: the score's order-preserving bits
@@ -156,39 +160,42 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
       };
       for (int f = tid; f < nn; f += kRevealNT) skeys[f] = score_key(scores[cell32(f)]);
       __syncthreads();
-      // 2-bit radix select of the kk-th largest key H, MSB first: each round
-      // every warp counts, among its keys that match H above the current digit,
-      // those whose digit is >= 1, 2 and 3; warp 0 adds the warps' counts, picks
-      // the digit and publishes the new prefix (two barriers a round, no atomics)
-      uint32_t H = 0u;
+      // 2-bit radix select of the kk-th largest key H, MSB first, by the first
+      // kSelWarps warps alone (a named barrier of their threads is much cheaper
+      // than a block barrier): each round every selecting warp counts, among its
+      // keys that match H above the current digit, those whose digit is >= 1, 2
+      // and 3, publishes the sums in this round's slots, and after the barrier
+      // adds all the warps' sums and picks the same digit (no atomics; the slots
+      // alternate between rounds, so one barrier a round suffices)
+      if (wid < kSelWarps) {
+        uint32_t H = 0u;
+        int need = kk, eq = nn, par = 0;
 #pragma unroll 1
-      for (int shift = 30; shift >= 0; shift -= 2) {
-        int c1 = 0, c2 = 0, c3 = 0;
-        const uint32_t hi_mask = (shift == 30) ? 0u : (0xffffffffu << (shift + 2));
-        for (int f = tid; f < nn; f += kRevealNT) {
-          const uint32_t key = skeys[f];
-          if ((key & hi_mask) == (H & hi_mask)) {
-            const uint32_t d = (key >> shift) & 3u;
-            c1 += d >= 1u;
-            c2 += d >= 2u;
-            c3 += d >= 3u;
+        for (int shift = 30; shift >= 0; shift -= 2) {
+          int c1 = 0, c2 = 0, c3 = 0;
+          const uint32_t hi_mask = (shift == 30) ? 0u : (0xffffffffu << (shift + 2));
+          for (int f = tid; f < nn; f += kSelWarps * 32) {
+            const uint32_t key = skeys[f];
+            if ((key & hi_mask) == (H & hi_mask)) {
+              const uint32_t d = (key >> shift) & 3u;
+              c1 += d >= 1u;
+              c2 += d >= 2u;
+              c3 += d >= 3u;
+            }
           }
-        }
-        c1 = __reduce_add_sync(0xffffffffu, c1);
-        c2 = __reduce_add_sync(0xffffffffu, c2);
-        c3 = __reduce_add_sync(0xffffffffu, c3);
-        if (lane == 0) {
-          slots[0][wid][0] = c1;
-          slots[0][wid][1] = c2;
-          slots[0][wid][2] = c3;
-        }
-        __syncthreads();
-        if (wid == 0) {
-          const int4 v = (lane < kRevealNT / 32) ? *reinterpret_cast<const int4*>(slots[0][lane]) : make_int4(0, 0, 0, 0);
+          c1 = __reduce_add_sync(0xffffffffu, c1);
+          c2 = __reduce_add_sync(0xffffffffu, c2);
+          c3 = __reduce_add_sync(0xffffffffu, c3);
+          if (lane == 0) {
+            slots[par][wid][0] = c1;
+            slots[par][wid][1] = c2;
+            slots[par][wid][2] = c3;
+          }
+          asm volatile("bar.sync 1, %0;" ::"n"(kSelWarps * 32) : "memory");
+          const int4 v = (lane < kSelWarps) ? *reinterpret_cast<const int4*>(slots[par][lane]) : make_int4(0, 0, 0, 0);
           const int C1 = __reduce_add_sync(0xffffffffu, v.x), C2 = __reduce_add_sync(0xffffffffu, v.y),
                     C3 = __reduce_add_sync(0xffffffffu, v.z);
-          int need = (shift == 30) ? kk : s_need;
-          int eq = (shift == 30) ? nn : s_eq;
+          par ^= 1;
           uint32_t d;
           if (C3 >= need) {
             d = 3u;
@@ -206,16 +213,16 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
             need -= C1;
             eq = eq - C1;
           }
-          __syncwarp();
-          if (lane == 0) {
-            s_prefix = (unsigned long long)(H | (d << shift));
-            s_need = need;
-            s_eq = eq;
-          }
+          H |= d << shift;
         }
-        __syncthreads();
-        H = (uint32_t)s_prefix;
+        if (tid == 0) {
+          s_prefix = (unsigned long long)H;
+          s_need = need;
+          s_eq = eq;
+        }
       }
+      __syncthreads();
+      const uint32_t H = (uint32_t)s_prefix;
       const int need = s_need;
       const int eq_cnt = s_eq;
       // every key above H is revealed; of the eq_cnt keys equal to H, the first

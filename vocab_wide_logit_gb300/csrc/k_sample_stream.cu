@@ -200,7 +200,6 @@ __global__ void __launch_bounds__(NT, 3)
   const long long n_clusters = (long long)gridDim.x / cs;
   const long long cluster_id = (long long)blockIdx.x / cs;
   const int P = a.P, V = a.V;
-  const float2 neg1 = make_float2(-1.f, -1.f);
   const float2 l2e = make_float2(kLog2e, kLog2e);
   int parity = 0;
 
@@ -262,7 +261,7 @@ __global__ void __launch_bounds__(NT, 3)
     }
     const bool guided = g != 0.f;
     const bool sampled = tau > 0.f;
-    const float2 g2 = make_float2(g, g);
+    const float2 ng2 = make_float2(-g, -g);
     const uint32_t t32 = (uint32_t)t;
     const uint32_t ctr3 = cur.iter_hi | (uint32_t)c;
     const int k = cur.k;
@@ -465,8 +464,13 @@ __global__ void __launch_bounds__(NT, 3)
           for (int i = 0; i < 4; ++i) {
             const float2 cp = make_float2(bf_lo(wc[i]), bf_hi(wc[i]));
             const uint32_t wu = (i == 0) ? vu[uu].x : (i == 1) ? vu[uu].y : (i == 2) ? vu[uu].z : vu[uu].w;
-            const float2 up = make_float2(bf_lo(wu), bf_hi(wu));
-            const float2 zg = __ffma2_rn(g2, __ffma2_rn(up, neg1, cp), cp);  // fl(c - u), then one fma
+            // fl(u - c), u widened to fp32 inside the subtraction; it is exactly
+            // -fl(c - u) (round to nearest is symmetric), so (-g) fl(u - c) + c in
+            // one fma is the combine fma(g, fl(c - u), c)
+            float dx, dy;
+            asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; sub.rn.f32.bf16 %0, lo, %3; sub.rn.f32.bf16 %1, hi, %4; }"
+                : "=f"(dx), "=f"(dy) : "r"(wu), "f"(cp.x), "f"(cp.y));
+            const float2 zg = __ffma2_rn(ng2, make_float2(dx, dy), cp);
             z[uu][i] = guided ? zg : cp;
           }
           if (CHECKED) {

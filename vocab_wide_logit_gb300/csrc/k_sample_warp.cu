@@ -164,7 +164,6 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (warp_min_blocks<NCH, FULL
     return;
   }
   const long long P_u = bt.tot_u;
-  const float2 neg1 = make_float2(-1.f, -1.f);
   const float2 l2e = make_float2(kLog2e, kLog2e);
 
   // position -> request walk over the warp's contiguous cell range (in marker
@@ -202,7 +201,7 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (warp_min_blocks<NCH, FULL
       const int ns = G.ns, sid = G.sid;
       // ---- step 1: z, row max, moments of chunks 0..NCH-2 (always full)
       float2 z[NCH][4];
-      const float2 g2 = make_float2(g, g);
+      const float2 ng2 = make_float2(-g, -g);
       float m0 = -kInf, m1 = -kInf;
       float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -215,8 +214,13 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (warp_min_blocks<NCH, FULL
         for (int i = 0; i < 4; ++i) {
           const float2 cp = make_float2(bf_lo(wc[i]), bf_hi(wc[i]));
           if (guided) {
-            const float2 up = make_float2(bf_lo(wu[i]), bf_hi(wu[i]));
-            z[j][i] = __ffma2_rn(g2, __ffma2_rn(up, neg1, cp), cp);  // fl(c - u), then one fma
+            // fl(u - c), u widened to fp32 inside the subtraction; it is exactly
+            // -fl(c - u) (round to nearest is symmetric), so (-g) fl(u - c) + c in
+            // one fma is the combine fma(g, fl(c - u), c)
+            float dx, dy;
+            asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; sub.rn.f32.bf16 %0, lo, %3; sub.rn.f32.bf16 %1, hi, %4; }"
+                : "=f"(dx), "=f"(dy) : "r"(wu[i]), "f"(cp.x), "f"(cp.y));
+            z[j][i] = __ffma2_rn(ng2, make_float2(dx, dy), cp);
           } else {
             z[j][i] = cp;
           }

@@ -49,7 +49,7 @@ def test_reveal_after_sampling_config3():
     assert np.array_equal(got[1], want[1])
 
 
-@pytest.mark.parametrize("levels", [2, 5, 0])
+@pytest.mark.parametrize("levels", [2, 5, 40, 300, 0])
 def test_reveal_with_ties_and_signed_zeros(levels):
     """Requests of up to 4 x 2049 cells are ranked in shared memory; the 4 x 4500 one (18000 cells,
     above the staging budget) by the 64-bit select over global memory."""

@@ -6,10 +6,11 @@
 // top reveal_count. One CTA per request finds the reveal_count-th cell of the
 // order (score desc, flattened index asc) and scatters the tokens of the cells
 // up to it into the canvas. A request of at most kRevealStaged cells is staged
-// once in shared memory as 32-bit score keys: a 2-bit radix select (16 rounds
-// of counting by warp reductions, one barrier each, no atomics) finds the k-th
-// key H, and when cells tied at H straddle the cut, a binary search over the
-// flattened index finds the last one revealed. A larger request runs an exact
+// once in shared memory as 32-bit score keys: a 2-bit radix select (rounds of
+// counting by warp reductions, one barrier each, no atomics) narrows the k-th
+// key H until at most 64 keys share the chosen prefix; one warp then ranks
+// those keys against each other to settle H. When cells tied at H straddle the
+// cut, a binary search over the flattened index finds the last one revealed. A larger request runs an exact
 // 64-bit radix select (score key above the inverted flattened index, so keys
 // are distinct) over global memory.
 #include <climits>
@@ -29,6 +30,9 @@ constexpr int kRevealNT = 1024;
 // behind block barriers).
 constexpr int kSelWarps = 16;
 constexpr int kRevealStaged = 16384;  // cells staged in shared memory (64 KB of keys)
+// Once the keys that match the selected prefix number at most this many, one
+// warp finishes the select by ranking them against each other.
+constexpr int kCandMax = 64;
 
 // Larger key = earlier in the reveal order: the score's order-preserving bits
 // (-0 folded onto +0, so equal scores tie) above the inverted flattened index.
@@ -96,7 +100,8 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
   __shared__ int hist[256];
   __shared__ __align__(16) int slots[2][kRevealNT / 32][4];
   __shared__ unsigned long long s_prefix;
-  __shared__ int s_need, s_eq;
+  __shared__ int s_need, s_eq, s_cnt;
+  __shared__ uint32_t cand[kCandMax];
   extern __shared__ uint32_t skeys[];  // the staged request's score keys, in flattened order
   pdl_release();
   pdl_wait();
@@ -159,6 +164,7 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
         return (long long)c * P + roff + (long long)((unsigned)f - c * Tu);
       };
       for (int f = tid; f < nn; f += kRevealNT) skeys[f] = score_key(scores[cell32(f)]);
+      if (tid == 0) s_cnt = 0;
       __syncthreads();
       // 2-bit radix select of the kk-th largest key H, MSB first, by the first
       // kSelWarps warps alone (a named barrier of their threads is much cheaper
@@ -166,12 +172,15 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
       // keys that match H above the current digit, those whose digit is >= 1, 2
       // and 3, publishes the sums in this round's slots, and after the barrier
       // adds all the warps' sums and picks the same digit (no atomics; the slots
-      // alternate between rounds, so one barrier a round suffices)
+      // alternate between rounds, so one barrier a round suffices). As soon as
+      // at most kCandMax keys match the prefix chosen so far, those keys are
+      // gathered and warp 0 ranks them against each other, which settles the
+      // remaining digits at once.
       if (wid < kSelWarps) {
         uint32_t H = 0u;
-        int need = kk, eq = nn, par = 0;
+        int need = kk, eq = nn, par = 0, shift = 30;
 #pragma unroll 1
-        for (int shift = 30; shift >= 0; shift -= 2) {
+        for (;; shift -= 2) {
           int c1 = 0, c2 = 0, c3 = 0;
           const uint32_t hi_mask = (shift == 30) ? 0u : (0xffffffffu << (shift + 2));
           for (int f = tid; f < nn; f += kSelWarps * 32) {
@@ -214,6 +223,49 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
             eq = eq - C1;
           }
           H |= d << shift;
+          if (shift == 0 || eq <= kCandMax) break;
+        }
+        if (shift > 0) {
+          // gather the eq keys that match H above `shift`
+          const uint32_t mask = 0xffffffffu << shift;
+          for (int fb = wid * 32; fb < nn; fb += kSelWarps * 32) {
+            const int f = fb + lane;
+            const uint32_t key = f < nn ? skeys[f] : 0u;
+            const bool m = f < nn && (key & mask) == (H & mask);
+            const unsigned b = __ballot_sync(0xffffffffu, m);
+            if (b) {
+              int base = 0;
+              if (lane == 0) base = atomicAdd(&s_cnt, __popc(b));
+              base = __shfl_sync(0xffffffffu, base, 0);
+              const int pos = base + __popc(b & ((1u << lane) - 1u));
+              if (m && pos < kCandMax) cand[pos] = key;  // pos < eq <= kCandMax
+            }
+          }
+          asm volatile("bar.sync 1, %0;" ::"n"(kSelWarps * 32) : "memory");
+          if (wid == 0) {
+            // the need-th largest candidate is the one with fewer than need
+            // candidates above it and at least need at or above it
+            const bool on0 = lane < eq, on1 = lane + 32 < eq;
+            const uint32_t k0 = on0 ? cand[lane] : 0u, k1 = on1 ? cand[lane + 32] : 0u;
+            int gt0 = 0, ge0 = 0, gt1 = 0, ge1 = 0;
+#pragma unroll 4
+            for (int j = 0; j < eq; ++j) {
+              const uint32_t v = cand[j];
+              gt0 += v > k0;
+              ge0 += v >= k0;
+              gt1 += v > k1;
+              ge1 += v >= k1;
+            }
+            const unsigned b0 = __ballot_sync(0xffffffffu, on0 && gt0 < need && need <= ge0);
+            const unsigned b1 = __ballot_sync(0xffffffffu, on1 && gt1 < need && need <= ge1);
+            const bool use1 = b0 == 0u;  // every such candidate has the same key
+            const int src = __ffs(use1 ? b1 : b0) - 1;
+            H = __shfl_sync(0xffffffffu, use1 ? k1 : k0, src);
+            const int hgt = __shfl_sync(0xffffffffu, use1 ? gt1 : gt0, src);
+            const int hge = __shfl_sync(0xffffffffu, use1 ? ge1 : ge0, src);
+            need -= hgt;
+            eq = hge - hgt;
+          }
         }
         if (tid == 0) {
           s_prefix = (unsigned long long)H;

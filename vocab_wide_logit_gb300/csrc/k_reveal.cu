@@ -6,11 +6,13 @@
 // top reveal_count. One CTA per request finds the reveal_count-th cell of the
 // order (score desc, flattened index asc) and scatters the tokens of the cells
 // up to it into the canvas. A request of at most kRevealStaged cells is staged
-// once in shared memory as 32-bit score keys: a 2-bit radix select (rounds of
-// counting by warp reductions, one barrier each, no atomics) narrows the k-th
-// key H until at most 64 keys share the chosen prefix; one warp then ranks
-// those keys against each other to settle H. When cells tied at H straddle the
-// cut, a binary search over the flattened index finds the last one revealed. A larger request runs an exact
+// once in shared memory as 32-bit score keys. The top byte of the k-th key H
+// comes from a 256-bin histogram built while staging, the next byte from a
+// second histogram over the keys that share the first; 2-bit rounds (counting
+// by warp reductions, one barrier each) go on only while more than 64 keys
+// share the prefix, and one warp then ranks those keys against each other to
+// settle H. When cells tied at H straddle the cut, a binary search over the
+// flattened index finds the last one revealed. A larger request runs an exact
 // 64-bit radix select (score key above the inverted flattened index, so keys
 // are distinct) over global memory.
 #include <climits>
@@ -100,7 +102,9 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
   __shared__ int hist[256];
   __shared__ __align__(16) int slots[2][kRevealNT / 32][4];
   __shared__ unsigned long long s_prefix;
-  __shared__ int s_need, s_eq, s_cnt;
+  __shared__ int s_need, s_eq, s_cnt, s_bad;
+  __shared__ int hist2[256];
+  __shared__ long long s_off, s_tot;
   __shared__ uint32_t cand[kCandMax];
   extern __shared__ uint32_t skeys[];  // the staged request's score keys, in flattened order
   pdl_release();
@@ -109,46 +113,46 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
   int parity = 0;
 
   for (int r = blockIdx.x; r < B; r += gridDim.x) {
-    // the request's offset and the batch total (sums of non-negative int32, in 64 bits)
-    long long off = 0, tot = 0;
-    int bad = 0;
-    for (int j = tid; j < B; j += kRevealNT) {
-      const int T = seq_lens[j];
-      bad |= T < 0;
-      const long long Tc = T < 0 ? 0 : T;
-      tot += Tc;
-      if (j < r) off += Tc;
-    }
+    // the request's offset and the batch total (sums of non-negative int32, in
+    // 64 bits), by warp 0; the previous request ended at a block barrier, so the
+    // shared state is free
+    const int T = seq_lens[r];
+    long long k = reveal_counts[r];
+    if (wid == 0) {
+      long long off = 0, tot = 0;
+      int bad = 0;
+      for (int j = lane; j < B; j += 32) {
+        const int Tj = seq_lens[j];
+        bad |= Tj < 0;
+        const long long Tc = Tj < 0 ? 0 : Tj;
+        tot += Tc;
+        if (j < r) off += Tc;
+      }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      off += __shfl_xor_sync(0xffffffffu, off, o);
-      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      for (int o = 16; o > 0; o >>= 1) {
+        off += __shfl_xor_sync(0xffffffffu, off, o);
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      }
+      bad = __any_sync(0xffffffffu, bad);
+      if (lane == 0) {
+        s_off = off;
+        s_tot = tot;
+        s_bad = bad;
+        s_cnt = 0;
+      }
     }
-    bad = __any_sync(0xffffffffu, bad);
-    __syncthreads();  // the previous request is done with the slots
-    if (lane == 0) {
-      reinterpret_cast<long long*>(slots[0])[wid] = off;
-      reinterpret_cast<long long*>(slots[1])[wid] = tot;
-      hist[wid] = bad;
+    if (tid < 256) {
+      hist[tid] = 0;
+      hist2[tid] = 0;
     }
     __syncthreads();
-    off = 0;
-    tot = 0;
-    bad = 0;
-#pragma unroll
-    for (int w = 0; w < kRevealNT / 32; ++w) {
-      off += reinterpret_cast<const long long*>(slots[0])[w];
-      tot += reinterpret_cast<const long long*>(slots[1])[w];
-      bad |= hist[w];
-    }
-    if (bad || tot != (long long)P) {
+    const long long off = s_off, tot = s_tot;
+    if (s_bad || tot != (long long)P) {
       if (tid == 0 && r == (int)blockIdx.x) report(d_status, DS_DEV_ERR_LAYOUT);
       return;  // uniform across the CTA; the layout is invalid for every request
     }
     const long long roff = off;
-    const int T = seq_lens[r];
     const long long n = (long long)C * T;
-    long long k = reveal_counts[r];
     k = k < 0 ? 0 : (k > n ? n : k);
     auto cell_of = [&](long long f) -> long long {
       const long long c = f / T;
@@ -163,9 +167,46 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
         const unsigned c = (unsigned)f / Tu;
         return (long long)c * P + roff + (long long)((unsigned)f - c * Tu);
       };
-      for (int f = tid; f < nn; f += kRevealNT) skeys[f] = score_key(scores[cell32(f)]);
-      if (tid == 0) s_cnt = 0;
+      for (int f = tid; f < nn; f += kRevealNT) {
+        const uint32_t key = score_key(scores[cell32(f)]);
+        skeys[f] = key;
+        atomicAdd(&hist[key >> 24], 1);
+      }
       __syncthreads();
+      // the top two bytes of H from two 256-bin histograms: the first built while
+      // staging, the second over the keys that match the first byte (skipped when
+      // at most kCandMax keys share it)
+      if (wid == 0) {
+        int digit, above;
+        pick_digit(hist, kk, lane, digit, above);
+        if (digit >= 0) {
+          s_prefix = (unsigned long long)digit << 24;
+          s_need = kk - above;
+          s_eq = hist[digit];
+        }
+      }
+      __syncthreads();
+      int shift = 24;
+      if (s_eq > kCandMax) {
+        const uint32_t top = (uint32_t)s_prefix >> 24;
+        for (int f = tid; f < nn; f += kRevealNT) {
+          const uint32_t key = skeys[f];
+          if ((key >> 24) == top) atomicAdd(&hist2[(key >> 16) & 255u], 1);
+        }
+        __syncthreads();
+        if (wid == 0) {
+          int digit, above;
+          const int need0 = s_need;
+          pick_digit(hist2, need0, lane, digit, above);
+          if (digit >= 0) {
+            s_prefix |= (unsigned long long)digit << 16;
+            s_need = need0 - above;
+            s_eq = hist2[digit];
+          }
+        }
+        __syncthreads();
+        shift = 16;
+      }
       // 2-bit radix select of the kk-th largest key H, MSB first, by the first
       // kSelWarps warps alone (a named barrier of their threads is much cheaper
       // than a block barrier): each round every selecting warp counts, among its
@@ -177,12 +218,13 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
       // gathered and warp 0 ranks them against each other, which settles the
       // remaining digits at once.
       if (wid < kSelWarps) {
-        uint32_t H = 0u;
-        int need = kk, eq = nn, par = 0, shift = 30;
+        uint32_t H = (uint32_t)s_prefix;
+        int need = s_need, eq = s_eq, par = 0;
 #pragma unroll 1
-        for (;; shift -= 2) {
+        while (eq > kCandMax && shift > 0) {
+          shift -= 2;
           int c1 = 0, c2 = 0, c3 = 0;
-          const uint32_t hi_mask = (shift == 30) ? 0u : (0xffffffffu << (shift + 2));
+          const uint32_t hi_mask = 0xffffffffu << (shift + 2);
           for (int f = tid; f < nn; f += kSelWarps * 32) {
             const uint32_t key = skeys[f];
             if ((key & hi_mask) == (H & hi_mask)) {
@@ -223,7 +265,6 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
             eq = eq - C1;
           }
           H |= d << shift;
-          if (shift == 0 || eq <= kCandMax) break;
         }
         if (shift > 0) {
           // gather the eq keys that match H above `shift`

@@ -335,9 +335,10 @@ __global__ void __launch_bounds__(NT, 3)
     };
     // lowest z that can still win, given the best known score bound and m
     // (+inf at temperature 0: no race, nothing is staged)
+    // (never below -FLT_MAX, so a comparison with it also rejects -inf)
     auto cut_of = [&](float SA) -> float {
       const float sb = fmaxf(SA, __fmaf_rn(tau, g_min, m));
-      return (sampled && !stop) ? sb - score_eps(sb) - tgmax : kInf;
+      return (sampled && !stop) ? fmaxf(sb - score_eps(sb) - tgmax, -FLT_MAX) : kInf;
     };
     // drop live entries whose upper score fell below thr (in place, in order)
     auto prune = [&](float thr) {
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(NT, 3)
         hi = __fmaf_rn(tau, gb.y, v.x);
       }
       ne -= cnt;
-      const float wlo = warp_max(lo);
+      const float wlo = warp_max_r(lo);
       const float known = fmaxf(SAl, slot_sa());
       if (wlo > known) publish(wlo);
       SAl = fmaxf(known, wlo);
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(NT, 3)
       const float cut = cut_of(fmaxf(SAl, slot_sa()));
       uint32_t mk = 0u;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) mk |= (zz[j] >= cut && zz[j] > -kInf) ? (1u << j) : 0u;
+      for (int j = 0; j < 8; ++j) mk |= (zz[j] >= cut) ? (1u << j) : 0u;
       const int n = __popc(mk);
       const int ex = warp_excl_scan(n, lane);
       const int tot = __shfl_sync(0xffffffffu, ex + n, 31);
@@ -530,7 +531,7 @@ __global__ void __launch_bounds__(NT, 3)
           const float cut = cut_of(fmaxf(SAl, slot_sa()));
 #pragma unroll
           for (int uu = 0; uu < NCHK; ++uu) {
-            const bool hot = cmx[uu] >= cut && cmx[uu] > -kInf;
+            const bool hot = cmx[uu] >= cut;
             const unsigned b = __ballot_sync(0xffffffffu, hot);
             if (hot) {
               const int pos = ns + __popc(b & lt_mask);

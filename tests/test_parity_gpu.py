@@ -293,6 +293,38 @@ def test_exact_ties_at_max_and_at_cut(V):
     assert np.array_equal(tok, ref["argmax"])
 
 
+@pytest.mark.parametrize("V,ratio,zeros", [(1025, 0.1, 400), (20000, 0.3, 8000), (248320, 0.1, 30000)])
+def test_signed_zeros_tied_at_the_max_and_the_cut(V, ratio, zeros):
+    """The row's maximum is 0, held by more ids than the kept set, half of them -0 and half +0:
+    -0 and +0 are equal values, so the kept set is the smallest ids among them whatever their sign.
+    The candidate count overflows the fast paths, so the exact fallbacks (the one-warp kernel's
+    full pass, the staged cluster kernel) decide membership."""
+    dev = _dev()
+    C, T = 1, 3
+    rng = np.random.Generator(np.random.PCG64(5))
+    z = -1.0 - np.abs(rng.standard_normal((C, T, V))).astype(np.float32)
+    for t in range(T):
+        ids = rng.choice(V, size=zeros, replace=False)
+        signs = rng.integers(0, 2, size=zeros)
+        z[0, t, ids] = np.where(signs == 1, np.float32(-0.0), np.float32(0.0))
+    c = wl.to_bf16(z)
+    bits = wl.bf16_bits(c)
+    assert (bits == 0x8000).any() and (bits == 0).any()
+    for tau in (0.8, 0.0):
+        inp = wl.SampleInputs(name="signed zeros", C=C, V=V, seq_lens=np.array([T], np.int32),
+                              request_ids=np.array([31], np.int32), guidance=np.array([0.0], np.float32),
+                              temperature=np.array([tau], np.float32), top_ratio=ratio, seed=9, c_logits=c,
+                              u_logits=None)
+        d = Dev(inp, dev)
+        tok, lp = d.run(2, 0)
+        ref = oracle_cells(inp, 2, 0)
+        if tau > 0:
+            assert (ref["thresh_ties"] > 0).all()
+        compare(inp, tok, lp, ref, label="signed zeros V=%d tau=%g" % (V, tau))
+        if tau == 0:
+            assert np.array_equal(tok, ref["argmax"])
+
+
 def test_misaligned_rows_and_u_alignment_differing_from_c():
     """Rows that start at arbitrary 2-byte offsets, with u's rows aligned differently from c's.
     V = 8192 is a multiple of 8: with aligned buffers every row would start on a chunk boundary,

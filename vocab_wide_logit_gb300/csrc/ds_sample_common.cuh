@@ -141,8 +141,9 @@ __device__ __forceinline__ float2 gumbel_bounds(uint32_t x) {
 }
 
 // 64-bit composite key of (z, id): larger key = earlier in the order (z desc, id asc).
+// -0 is folded onto +0: the two are equal values, so they tie and the smaller id goes first.
 __device__ __forceinline__ unsigned long long rank_key(float z, int id) {
-  return ((unsigned long long)order_key(z) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)id);
+  return ((unsigned long long)order_key(z == 0.f ? 0.f : z) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)id);
 }
 
 }  // namespace ds

@@ -445,7 +445,9 @@ __global__ void __launch_bounds__(NT, 2) k_sample_cluster(const SampleArgs a, in
         if (sampled) {
           cnt += (v.x >= tlo) + (v.y >= tlo) + (v.z >= tlo) + (v.w >= tlo);
           chi += (v.x >= thi) + (v.y >= thi) + (v.z >= thi) + (v.w >= thi);
-        } else {
+        } else if (amin == INT_MAX) {
+          // a thread walks its elements in increasing id order: its first group
+          // holding the max holds its smallest id
           const int id4 = id_base + 4 * l4;
           if (v.w == m) amin = id4 + 3;
           if (v.z == m) amin = id4 + 2;

@@ -201,6 +201,29 @@ def test_config4_greedy_large_vocab():
                       "max_rel_dp": float(np.max(np.abs(p - p_ref) / p_ref))}
 
 
+@pytest.mark.parametrize("V", [1025, 248320])
+def test_greedy_signed_zeros_tied_at_the_max(V):
+    """Rows whose maximum 0 is held by +0 and -0 at scattered ids: the argmax is the smallest of
+    those ids whatever its sign, on one CTA and across a cluster's slices."""
+    dev = _dev()
+    rng = np.random.Generator(np.random.PCG64(8))
+    n = 8
+    x = -1.0 - np.abs(rng.standard_normal((n, V))).astype(np.float32)
+    for r in range(n):
+        ids = rng.choice(V, size=40, replace=False)
+        x[r, ids] = np.where(rng.integers(0, 2, size=40) == 1, np.float32(-0.0), np.float32(0.0))
+        if r % 2 == 0:
+            x[r, ids.min()] = np.float32(-0.0)  # the smallest id holds -0 in half the rows
+    xb = wl.to_bf16(x)
+    mx, lse, am = pkg.greedy_lse(xb.to(dev))
+    torch.cuda.synchronize()
+    ref = oracle.greedy_rows(wl.bf16_bits(xb), n, V)
+    assert np.array_equal(mx.cpu().numpy(), ref["max"])
+    assert np.array_equal(am.cpu().numpy(), ref["argmax"])
+    assert np.array_equal(am.cpu().numpy(), [np.flatnonzero(x[r] == 0).min() for r in range(n)])
+    assert np.max(np.abs(lse.cpu().numpy() - ref["lse"])) <= LOGPROB_TOL
+
+
 def test_config5_every_cell():
     """Full-size large-vocabulary launch (the benchmark's launch plan: single CTAs, then pairs for
     the last cells, then the exact pass over marked cells): every one of the 1024 cells at

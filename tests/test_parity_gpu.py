@@ -391,23 +391,38 @@ def test_warp_to_stream_switch_with_misaligned_rows(V):
     assert int(d.status.item()) == 0
 
 
-def test_neg_inf_logits():
+@pytest.mark.parametrize("V,ratio", [(1025, 0.1), (9000, 0.1), (9000, 0.3), (248320, 0.1)])
+def test_neg_inf_logits(V, ratio):
+    """Rows that are all -inf, rows with fewer finite values than k, and half-masked rows, on every
+    sample kernel (one warp per cell, the streaming pass, the staged cluster kernel)."""
     dev = _dev()
-    for V in (1025, 9000):
-        rng = np.random.Generator(np.random.PCG64(2))
-        z = (rng.standard_normal((1, 4, V)) * 2).astype(np.float32)
-        z[0, 0, :] = -np.inf                       # whole row -inf
-        z[0, 1, : V - 5] = -np.inf                 # fewer finite values than k
-        z[0, 2, ::2] = -np.inf                     # half masked
-        inp = wl.SampleInputs(name="inf", C=1, V=V, seq_lens=np.array([2, 2], np.int32),
-                              request_ids=np.array([5, 6], np.int32), guidance=np.array([0.0, 0.0], np.float32),
-                              temperature=np.array([0.9, 0.0], np.float32), top_ratio=0.1, seed=1,
-                              c_logits=wl.to_bf16(z), u_logits=None)
-        d = Dev(inp, dev)
-        tok, lp = d.run(3, 0)
-        ref = oracle_cells(inp, 3, 0)
-        compare(inp, tok, lp, ref, label="inf V=%d" % V)
-        assert tok[0] == 0 and np.isnan(lp[0])
+    rng = np.random.Generator(np.random.PCG64(2))
+    z = (rng.standard_normal((1, 4, V)) * 2).astype(np.float32)
+    z[0, 0, :] = -np.inf                       # whole row -inf
+    z[0, 1, : V - 5] = -np.inf                 # fewer finite values than k
+    z[0, 2, ::2] = -np.inf                     # half masked
+    inp = wl.SampleInputs(name="inf", C=1, V=V, seq_lens=np.array([2, 2], np.int32),
+                          request_ids=np.array([5, 6], np.int32), guidance=np.array([0.0, 0.0], np.float32),
+                          temperature=np.array([0.9, 0.0], np.float32), top_ratio=ratio, seed=1,
+                          c_logits=wl.to_bf16(z), u_logits=None)
+    d = Dev(inp, dev)
+    tok, lp = d.run(3, 0)
+    ref = oracle_cells(inp, 3, 0)
+    compare(inp, tok, lp, ref, label="inf V=%d ratio=%g" % (V, ratio))
+    assert tok[0] == 0 and np.isnan(lp[0])
+
+
+@pytest.mark.parametrize("V,ratio", [(1025, 0.1), (9000, 0.1), (9000, 0.3), (248320, 0.1)])
+def test_extreme_temperatures(V, ratio):
+    """Temperatures from 1e-20 (the noise is below fp32 resolution: near-ties, exempt) to 1e20
+    (the noise decides alone), guided and unguided, on every sample kernel."""
+    dev = _dev()
+    taus = [1e-20, 1e-6, 1e3, 1e20]
+    inp = wl.make_sample_inputs("tau", C=2, seq_lens=[3] * len(taus), V=V, guidance=[1.5, 0.0, 1.5, 0.0],
+                                temperature=taus, sigma_c=2.0, sigma_u=1.0, top_ratio=ratio, seed=12)
+    d = Dev(inp, dev)
+    tok, lp = d.run(5, 3)
+    compare(inp, tok, lp, oracle_cells(inp, 5, 3), label="temperatures V=%d ratio=%g" % (V, ratio))
 
 
 def test_repeat_calls_are_deterministic():

@@ -24,12 +24,11 @@ namespace ds {
 
 namespace {
 
-// A request holds about 2000 cells: 1024 threads give 2 keys per thread per
-// round (16.7 us per config-3 call, against 18.0 and 19.7 us at 512 and 256).
+// A request holds about 800-3200 cells: 1024 threads stage them in one to four
+// loads each (512 and 256 threads measured slower when the select ran 16 rounds).
 constexpr int kRevealNT = 1024;
-// Warps that run the select rounds: 16 (15.0 us per config-3 call on the
-// device, against 17.4, 22.0 and 33.1 us with 8, 4 and 2, and 16.4 us with all 32
-// behind block barriers).
+// Warps that run the 2-bit rounds: 16 behind a named barrier of their own (with
+// all 16 rounds, 16 warps beat 8, 4 and 2 warps and all 32 behind block barriers).
 constexpr int kSelWarps = 16;
 constexpr int kRevealStaged = 16384;  // cells staged in shared memory (64 KB of keys)
 // Once the keys that match the selected prefix number at most this many, one

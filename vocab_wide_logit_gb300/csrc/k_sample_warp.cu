@@ -120,7 +120,11 @@ constexpr int warp_min_blocks() {
 // FULL = false: the lean pass (marks what it cannot settle with kStreamMark).
 // FULL = true: every path; with only_marked set its warps scan their cell
 // ranges for marks and finish just those cells.
-template <int NCH, bool FULL>
+// RAISE (lean pass of calls with per-request ratios, where k reaches the list's
+// capacity): a first threshold that keeps more than kDenseCap candidates is
+// raised once instead of leaving the cell to the exact pass. Calls with one ratio
+// for every request run without it: the extra path costs them about 1%.
+template <int NCH, bool FULL, bool RAISE>
 __global__ void __launch_bounds__(kWarpKernelThreads, (warp_min_blocks<NCH, FULL>()))
     k_sample_warp(const SampleArgs a, int only_marked) {
   pdl_release();
@@ -335,17 +339,25 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (warp_min_blocks<NCH, FULL
             ca += (zs1 >= tlo) ? 256u : 0u;  // zs1 is -inf for lanes without a scalar element
             cnt = (int)((ca - col0) >> 8);
             ctot = warp_sum_i(cnt);
-            if (!guessed || ctot >= k || attempt == (FULL ? 2 : 1)) break;
+            // the lean kernel's list holds kDenseCap candidates: more than that
+            // raises the threshold once, toward the middle of [k, kDenseCap]
+            const bool over = RAISE && ctot > kDenseCap;
+            if (!guessed || (ctot >= k && !over) || attempt == (FULL ? 2 : 1)) break;
             // lower the threshold by the shortfall (and a dozen more) over the
             // normal density at the first guess; the full kernel's third
             // attempt keeps every finite element
-            float lower = -FLT_MAX;
+            float next = -FLT_MAX;
             if (attempt == 0 && sd > 0.f) {
               const float qe = (tlo - mu) / sd;
               const float dens = (float)a.V * 0.39894228f * __expf(-0.5f * qe * qe) / sd;
-              lower = tlo - (float)(k + 12 - ctot) / dens;
+              next = over ? tlo + (float)(ctot - (k + kDenseCap) / 2) / dens : tlo - (float)(k + 12 - ctot) / dens;
             }
-            tlo = (lower < tlo && lower > -FLT_MAX) ? lower : -FLT_MAX;
+            if (over) {
+              if (!(next > tlo)) break;  // no raise possible: the cell is left to the exact pass
+              tlo = next;
+            } else {
+              tlo = (next < tlo && next > -FLT_MAX) ? next : -FLT_MAX;
+            }
           }
           __syncwarp();
           if (!FULL && (ctot < k || ctot > kDenseCap)) {
@@ -413,10 +425,10 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (warp_min_blocks<NCH, FULL
 }
 
 // ---------------------------------------------------------------- launcher
-template <int NCH, bool FULL>
+template <int NCH, bool FULL, bool RAISE = false>
 static cudaError_t launch_nch(const SampleArgs& a, cudaStream_t st, int num_sms, int only_marked) {
   const size_t smem = (size_t)(kWarpKernelThreads / 32) * sizeof(WarpSmem<NCH>);
-  auto kern = k_sample_warp<NCH, FULL>;
+  auto kern = k_sample_warp<NCH, FULL, RAISE>;
   const int per_sm = cached(reinterpret_cast<const void*>(kern), (long long)smem, [&](int) {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     int n = 0;
@@ -451,6 +463,17 @@ int warp_kernel_max_vocab() { return 8 * 256 + 7; }
 template <bool FULL>
 static cudaError_t launch_warp_variant(const SampleArgs& a, cudaStream_t st, int num_sms, int only_marked) {
   const int nch = ((a.V >> 3) + 31) / 32;
+  if (!FULL && a.ratios) {  // k varies by request and can fill the list (V >= 520)
+    switch (nch) {
+      case 3: return launch_nch<3, false, true>(a, st, num_sms, only_marked);
+      case 4: return launch_nch<4, false, true>(a, st, num_sms, only_marked);
+      case 5: return launch_nch<5, false, true>(a, st, num_sms, only_marked);
+      case 6: return launch_nch<6, false, true>(a, st, num_sms, only_marked);
+      case 7: return launch_nch<7, false, true>(a, st, num_sms, only_marked);
+      case 8: return launch_nch<8, false, true>(a, st, num_sms, only_marked);
+      default: break;
+    }
+  }
   switch (nch < 1 ? 1 : nch) {
     case 1: return launch_nch<1, FULL>(a, st, num_sms, only_marked);
     case 2: return launch_nch<2, FULL>(a, st, num_sms, only_marked);

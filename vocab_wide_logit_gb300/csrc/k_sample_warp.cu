@@ -117,6 +117,75 @@ constexpr int warp_min_blocks() {
   return (NCH <= 4) ? (FULL ? DS_WARP_MINB : DS_WARP_LEAN_MINB) : ((NCH <= 6) ? 3 : 2);
 }
 
+
+// Cell weights for the lean pass with per-request ratios: a request's cells cost
+// about the same up to some 130 kept ids (the candidates fit the 5-slot
+// straight-line race) and about 0.75% more per kept id above that (longer races
+// and lists; measured at V = 1025: k = 205 costs 1.56 times k = 103).
+__device__ __forceinline__ long long cell_weight(const SampleArgs& a, int r) {
+  const float ratio = a.ratios[r];
+  int kk = 1;
+  if (ratio > 0.f && ratio <= 1.f) kk = min(max((int)ceilf(ratio * (float)a.V), 1), a.V);
+  return 128 + max(0, kk - 130);
+}
+
+// Weight of one row of cells (every position once), by the whole warp.
+__device__ __forceinline__ long long row_weight(const SampleArgs& a, int lane) {
+  long long R = 0;
+  for (int base = 0; base < a.B; base += 32) {
+    const int r = base + lane;
+    long long tw = 0;
+    if (r < a.B) tw = (long long)max(a.seq_lens[r], 0) * cell_weight(a, r);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tw += __shfl_xor_sync(0xffffffffu, tw, o);
+    R += tw;
+  }
+  return R;
+}
+
+// The first cell whose cumulative weight (cells in (c, p) order) reaches x,
+// for 0 <= x <= C R; every lane returns the same cell.
+__device__ long long cell_at_weight(const SampleArgs& a, long long x, long long R, int lane) {
+  const long long c = x / R;
+  if (c >= a.C) return (long long)a.C * a.P;
+  const long long rem = x - c * R;
+  long long acc = 0;
+  int off = 0;
+  for (int base = 0; base < a.B; base += 32) {
+    const int r = base + lane;
+    int T = 0;
+    long long w = 1;
+    if (r < a.B) {
+      T = max(a.seq_lens[r], 0);
+      w = cell_weight(a, r);
+    }
+    const long long tw = (long long)T * w;
+    long long inc = tw;
+    int incT = T;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, inc, o);
+      const int tT = __shfl_up_sync(0xffffffffu, incT, o);
+      if (lane >= o) {
+        inc += t;
+        incT += tT;
+      }
+    }
+    const long long ex = inc - tw;
+    const bool here = r < a.B && T > 0 && rem >= acc + ex && rem < acc + inc;
+    const unsigned b = __ballot_sync(0xffffffffu, here);
+    if (b) {
+      // the first of this request's cells whose start weight reaches rem
+      const long long t = (rem - acc - ex + w - 1) / w;
+      const long long p = (long long)off + (incT - T) + t;
+      return c * a.P + __shfl_sync(0xffffffffu, p, __ffs(b) - 1);
+    }
+    acc += __shfl_sync(0xffffffffu, inc, 31);
+    off += __shfl_sync(0xffffffffu, incT, 31);
+  }
+  return (c + 1) * a.P;
+}
+
 // FULL = false: the lean pass (marks what it cannot settle with kStreamMark).
 // FULL = true: every path; with only_marked set its warps scan their cell
 // ranges for marks and finish just those cells.
@@ -136,9 +205,9 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (warp_min_blocks<NCH, FULL
   const long long n_cells = (long long)a.C * a.P;
   const long long nw = (long long)gridDim.x * (kWarpKernelThreads / 32);
   const long long gw = (long long)blockIdx.x * (kWarpKernelThreads / 32) + (threadIdx.x >> 5);
-  const long long cbeg = gw * n_cells / nw;
-  const long long cend = (gw + 1) * n_cells / nw;
-  if (cbeg >= cend) return;
+  long long cbeg = gw * n_cells / nw;
+  long long cend = (gw + 1) * n_cells / nw;
+  if (!RAISE && cbeg >= cend) return;
 
   const bool marked_only = FULL && only_marked;
   // first cell at or after `from` in this warp's range that the lean pass marked
@@ -164,8 +233,20 @@ __global__ void __launch_bounds__(kWarpKernelThreads, (warp_min_blocks<NCH, FULL
       a.out_tokens[cell] = -1;
       a.out_logprobs[cell] = __int_as_float(0x7fc00000);
     }
-    if (lane == 0) report(a.d_status, DS_DEV_ERR_LAYOUT);
+    if (lane == 0 && cbeg < cend) report(a.d_status, DS_DEV_ERR_LAYOUT);
     return;
+  }
+  if (RAISE) {
+    // ranges of equal estimated cost instead of equal cell counts: with per-request
+    // ratios the expensive requests would otherwise set the pass's time
+    const long long R = row_weight(a, lane);
+    const long long total = R * a.C;
+    if (R > 0) {
+      cbeg = cell_at_weight(a, gw * total / nw, R, lane);
+      cend = (gw + 1 == nw) ? n_cells : cell_at_weight(a, (gw + 1) * total / nw, R, lane);
+    }
+    if (cbeg >= cend) return;
+    cell0 = cbeg;
   }
   const long long P_u = bt.tot_u;
   const float2 l2e = make_float2(kLog2e, kLog2e);

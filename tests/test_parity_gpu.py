@@ -536,6 +536,46 @@ def test_per_request_ratio_and_iteration(V):
     compare(inp, tok.cpu().numpy().reshape(-1), lp.cpu().numpy().reshape(-1), ref, label="per-request V%d" % V)
 
 
+@pytest.mark.parametrize("V", [520, 1025, 2048])
+def test_per_request_ratios_near_the_list_capacity(V):
+    """One-warp-per-cell kernel with per-request ratios whose candidate counts reach the
+    256-entry list (its first threshold is then raised once) and with requests of very
+    different cost (warps take ranges of equal estimated cost): every cell against the oracle,
+    with and without the exact pass."""
+    dev = _dev()
+    B = 12
+    rng = np.random.Generator(np.random.PCG64(V + 5))
+    seq = rng.integers(20, 200, size=B).astype(np.int32)
+    g = np.where(np.arange(B) % 3 == 0, 0.0, 1.5).astype(np.float32)
+    tau = np.full(B, 0.9, np.float32)
+    inp = wl.make_sample_inputs("cap%d" % V, 4, seq, V, g, tau, 2.5, 1.0, 0.1, seed=V + 2)
+    ratios = np.array([0.2, 0.24, 0.05, 0.1, 0.3, 0.15, 0.24, 0.01, 0.2, 0.12, 0.25, 0.08], np.float32)
+    iters = rng.integers(0, 1 << 20, size=B).astype(np.uint32)
+    d = Dev(inp, dev)
+    tr = torch.from_numpy(ratios).to(dev)
+    ti = torch.from_numpy(iters.view(np.int32)).to(dev)
+    ref = oracle.sample_cells(inp.request_ids, wl.bf16_bits(inp.c_logits), wl.bf16_bits(inp.u_logits),
+                              inp.seq_lens, inp.C, inp.P, inp.V, inp.guidance, inp.temperature, 0.5, inp.seed, 0,
+                              top_ratios=ratios, iterations=iters)
+    for flags in (0, pkg.DS_FLAG_SKIP_EXACT_PASS):
+        tok = torch.full((inp.C, inp.P), -7, dtype=torch.int32, device=dev)
+        lp = torch.full((inp.C, inp.P), 7.0, dtype=torch.float32, device=dev)
+        pkg.ds_sample(d.rid, d.c, d.u, d.sl, d.g, d.tau, 0.5, inp.seed, 0, tok, lp, d_status=d.status,
+                      top_ratios=tr, iterations=ti, flags=flags)
+        torch.cuda.synchronize()
+        assert int(d.status.item()) == 0
+        t, l = tok.cpu().numpy().reshape(-1), lp.cpu().numpy().reshape(-1)
+        if flags:
+            # without the exact pass, the cells left to it carry the mark and every other
+            # cell is already final
+            done = np.nonzero(t != pkg.DS_MARKED)[0]
+            assert (t >= -2).all() and len(done) > 0
+            compare(inp, t, l, {k: v[done] for k, v in ref.items()}, cells=done,
+                    label="capacity V%d, lean pass only" % V)
+        else:
+            compare(inp, t, l, ref, label="capacity V%d" % V)
+
+
 def test_per_request_invalid_ratio_is_reported_per_request():
     dev = _dev()
     inp = wl.make_sample_inputs("bad_ratio", 2, [4, 5], 1025, [2.0, 2.0], [0.9, 0.9], 3.0, 1.5, 0.1, seed=3)

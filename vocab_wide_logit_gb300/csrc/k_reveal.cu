@@ -30,7 +30,7 @@ constexpr int kRevealNT = 1024;
 // Warps that run the 2-bit rounds: 16 behind a named barrier of their own (with
 // all 16 rounds, 16 warps beat 8, 4 and 2 warps and all 32 behind block barriers).
 constexpr int kSelWarps = 16;
-constexpr int kRevealStaged = 16384;  // cells staged in shared memory (64 KB of keys)
+constexpr int kRevealStaged = 16384;  // cells staged in shared memory (64 KB of keys, 64 KB of tokens)
 // Once the keys that match the selected prefix number at most this many, one
 // warp finishes the select by ranking them against each other.
 constexpr int kCandMax = 64;
@@ -105,7 +105,9 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
   __shared__ int hist2[256];
   __shared__ long long s_off, s_tot;
   __shared__ uint32_t cand[kCandMax];
-  extern __shared__ uint32_t skeys[];  // the staged request's score keys, in flattened order
+  extern __shared__ uint32_t skeys[];  // the staged request's score keys, in flattened order,
+                                       // then its tokens (kRevealStaged entries each)
+  int32_t* stok = reinterpret_cast<int32_t*>(skeys + kRevealStaged);
   pdl_release();
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -167,7 +169,9 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
         return (long long)c * P + roff + (long long)((unsigned)f - c * Tu);
       };
       for (int f = tid; f < nn; f += kRevealNT) {
-        const uint32_t key = score_key(scores[cell32(f)]);
+        const long long cell = cell32(f);
+        const uint32_t key = score_key(scores[cell]);
+        stok[f] = tokens[cell];  // loaded now, with the score, so the scatter waits on no load
         skeys[f] = key;
         atomicAdd(&hist[key >> 24], 1);
       }
@@ -341,7 +345,7 @@ __global__ void __launch_bounds__(kRevealNT) k_reveal(const float* __restrict__ 
         const uint32_t key = skeys[f];
         const bool on = key > H || (key == H && f < f_cut);
         const long long cell = cell32(f);
-        if (on) canvas[cell] = tokens[cell];
+        if (on) canvas[cell] = stok[f];
         if (revealed) revealed[cell] = on ? 1 : 0;
       }
       __syncthreads();  // skeys is restaged by the next request
@@ -394,7 +398,7 @@ cudaError_t launch_reveal(const float* scores, const int32_t* tokens, const int3
   if (sms <= 0) return cudaErrorUnknown;
   const int ok = cached(reinterpret_cast<const void*>(k_reveal), 0, [](int) {
     const cudaError_t r = cudaFuncSetAttribute(k_reveal, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)(kRevealStaged * sizeof(uint32_t)));
+                                               (int)(2 * kRevealStaged * sizeof(uint32_t)));
     return r == cudaSuccess ? 1 : -(int)r;
   });
   if (ok <= 0) return ok < 0 ? (cudaError_t)(-ok) : cudaErrorUnknown;
@@ -405,7 +409,7 @@ cudaError_t launch_reveal(const float* scores, const int32_t* tokens, const int3
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks, 1, 1);
   cfg.blockDim = dim3(kRevealNT, 1, 1);
-  cfg.dynamicSmemBytes = kRevealStaged * sizeof(uint32_t);
+  cfg.dynamicSmemBytes = 2 * kRevealStaged * sizeof(uint32_t);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
